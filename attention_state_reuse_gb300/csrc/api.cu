@@ -1,0 +1,395 @@
+// C ABI entry points: argument validation, TMA descriptor set-up and kernel launches.
+//
+// One attention-layer step (DiTango, gist.science/paper/2607.15650, Methodology 1-2):
+//   1. validate the reuse mask against the plan's cache bookkeeping (host);
+//   2. optional 3D RoPE of q and k into the caller's workspace (rope.cu);
+//   3. fresh states for the computed pairs only, written into the state cache (pair_tc.cu for
+//      bf16, pair_f32.cu for fp32), over a schedule that lists computed pairs only;
+//   4. merge of all P cached states of every query row (merge.cu);
+//   5. record the computed pairs as valid at this step.
+// Every device buffer belongs to the caller; nothing here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "ditango_internal.h"
+#include "plan_internal.h"
+
+namespace ditango {
+namespace {
+
+// Set by kernels when a bounded barrier wait gives up; read and cleared by
+// ditango_device_status.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int* err_ptr = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DITANGO_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DITANGO_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return DITANGO_ERR_CUDA;
+    d.err_ptr = static_cast<int*>(p);
+    d.ready = true;
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        fn == nullptr)
+      return DITANGO_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = &d;
+  return DITANGO_OK;
+}
+
+size_t elem_size(int32_t dtype) { return dtype == DITANGO_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks a [B, N, H, d] tensor with d contiguous.
+int check_bnhd(const ditango_tensor* t, int64_t B, int64_t N, int64_t H, int64_t d, int32_t dtype) {
+  if (t == nullptr || t->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (t->ndim != 4) return DITANGO_ERR_SHAPE;
+  if (t->shape[0] != B || t->shape[1] != N || t->shape[2] != H || t->shape[3] != d)
+    return DITANGO_ERR_SHAPE;
+  if (t->dtype != dtype) return DITANGO_ERR_DTYPE;
+  if (t->stride[3] != 1) return DITANGO_ERR_SHAPE;
+  const int64_t vec = 16 / static_cast<int64_t>(elem_size(dtype));
+  if (!aligned16(t->ptr)) return DITANGO_ERR_ALIGN;
+  for (int a = 0; a < 3; ++a)
+    if (t->stride[a] <= 0 || t->stride[a] % vec != 0) return DITANGO_ERR_ALIGN;
+  return DITANGO_OK;
+}
+
+bool contiguous(const ditango_tensor* t) {
+  int64_t s = 1;
+  for (int a = t->ndim - 1; a >= 0; --a) {
+    if (t->shape[a] != 1 && t->stride[a] != s) return false;
+    s *= t->shape[a];
+  }
+  return true;
+}
+
+int encode_bnhd_map(CUtensorMap* map, const void* ptr, const int64_t* shape, const int64_t* stride) {
+  // dims innermost first: d, H, N, B; byte strides of H, N, B
+  const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(shape[3]), static_cast<cuuint64_t>(shape[2]),
+                              static_cast<cuuint64_t>(shape[1]), static_cast<cuuint64_t>(shape[0])};
+  const cuuint64_t gstr[3] = {static_cast<cuuint64_t>(stride[2]) * 2,
+                              static_cast<cuuint64_t>(stride[1]) * 2,
+                              static_cast<cuuint64_t>(stride[0]) * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), gdim,
+                              gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DITANGO_OK : DITANGO_ERR_CUDA;
+}
+
+int check_rope(const ditango_rope* r, int64_t N, int64_t d) {
+  if (r->dt < 0 || r->dh < 0 || r->dw < 0 || (r->dt | r->dh | r->dw) & 1)
+    return DITANGO_ERR_INVALID_ARG;
+  if (r->dt + r->dh + r->dw != d) return DITANGO_ERR_SHAPE;
+  if (r->Hl < 1 || r->Wl < 1 || r->T_tab < 1 || r->start_frame < 0) return DITANGO_ERR_INVALID_ARG;
+  if (N % (r->Hl * r->Wl) != 0) return DITANGO_ERR_SHAPE;
+  if (r->start_frame + N / (r->Hl * r->Wl) > r->T_tab) return DITANGO_ERR_SHAPE;
+  if ((r->dt && (!r->cos_t || !r->sin_t)) || (r->dh && (!r->cos_h || !r->sin_h)) ||
+      (r->dw && (!r->cos_w || !r->sin_w)))
+    return DITANGO_ERR_INVALID_ARG;
+  return DITANGO_OK;
+}
+
+size_t rope_workspace_bytes(int64_t B, int64_t N, int64_t H, int64_t d, int32_t dtype) {
+  const size_t one = static_cast<size_t>(B * N * H * d) * elem_size(dtype);
+  const size_t one_aligned = (one + 255) & ~static_cast<size_t>(255);
+  return 2 * one_aligned;
+}
+
+}  // namespace
+}  // namespace ditango
+
+using namespace ditango;
+
+extern "C" {
+
+size_t ditango_attn_step_workspace_size(ditango_plan_t plan, int64_t B, int64_t H, int32_t d,
+                                        int32_t dtype, int32_t use_rope) {
+  if (plan == nullptr || !use_rope) return 0;
+  return rope_workspace_bytes(B, plan->N, H, d, dtype);
+}
+
+int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditango_tensor* k,
+                      const ditango_tensor* v, const ditango_rope* rope,
+                      const uint8_t* reuse_mask, const ditango_state_cache* cache,
+                      const ditango_tensor* out, const ditango_tensor* out_lse,
+                      float softmax_scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (plan == nullptr || q == nullptr || k == nullptr || v == nullptr || cache == nullptr ||
+      out == nullptr)
+    return DITANGO_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return DITANGO_ERR_INVALID_ARG;
+  if (q->ptr == nullptr || q->ndim != 4) return q->ptr == nullptr ? DITANGO_ERR_INVALID_ARG : DITANGO_ERR_SHAPE;
+  const int64_t B = q->shape[0], N = q->shape[1], H = q->shape[2], d = q->shape[3];
+  const int32_t dtype = q->dtype;
+  const int64_t P = plan->P;
+  if (dtype != DITANGO_BF16 && dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  if (N != plan->N || B < 1 || H < 1) return DITANGO_ERR_SHAPE;
+  if (d != 64 && d != 128) return DITANGO_ERR_UNSUPPORTED;
+  if (B * H * N > (int64_t{1} << 31)) return DITANGO_ERR_SHAPE;
+  int st;
+  if ((st = check_bnhd(q, B, N, H, d, dtype)) != DITANGO_OK) return st;
+  if ((st = check_bnhd(k, B, N, H, d, dtype)) != DITANGO_OK) return st;
+  if ((st = check_bnhd(v, B, N, H, d, dtype)) != DITANGO_OK) return st;
+  if ((st = check_bnhd(out, B, N, H, d, dtype)) != DITANGO_OK) return st;
+  if (out_lse != nullptr) {
+    if (out_lse->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+    if (out_lse->dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+    if (out_lse->ndim != 3 || out_lse->shape[0] != B || out_lse->shape[1] != H ||
+        out_lse->shape[2] != N)
+      return DITANGO_ERR_SHAPE;
+  }
+  const ditango_tensor& cO = cache->O;
+  const ditango_tensor& cL = cache->lse;
+  if (cO.ptr == nullptr || cL.ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (cO.dtype != dtype || cL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  if (cO.ndim != 5 || cO.shape[0] != B || cO.shape[1] != H || cO.shape[2] != P ||
+      cO.shape[3] != N || cO.shape[4] != d || !contiguous(&cO))
+    return DITANGO_ERR_SHAPE;
+  if (cL.ndim != 4 || cL.shape[0] != B || cL.shape[1] != H || cL.shape[2] != P ||
+      cL.shape[3] != N || !contiguous(&cL))
+    return DITANGO_ERR_SHAPE;
+  if (!aligned16(cO.ptr) || !aligned16(cL.ptr)) return DITANGO_ERR_ALIGN;
+  if (rope != nullptr) {
+    if ((st = check_rope(rope, N, d)) != DITANGO_OK) return st;
+    const size_t need = rope_workspace_bytes(B, N, H, d, dtype);
+    if (workspace == nullptr || workspace_bytes < need) return DITANGO_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DITANGO_ERR_ALIGN;
+  }
+  if ((st = plan_validate(plan, reuse_mask)) != DITANGO_OK) return st;
+  const uint8_t* mask = plan_effective_mask(plan, reuse_mask);
+
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != DITANGO_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // ---- 1. rotary prologue into the workspace
+  const void* qp = q->ptr;
+  const void* kp = k->ptr;
+  int64_t qs[4] = {q->stride[0], q->stride[1], q->stride[2], 1};
+  int64_t ks[4] = {k->stride[0], k->stride[1], k->stride[2], 1};
+  if (rope != nullptr) {
+    const size_t one = rope_workspace_bytes(B, N, H, d, dtype) / 2;
+    RopeApplyArgs ra;
+    std::memset(&ra, 0, sizeof(ra));
+    ra.n_tensors = 2;
+    ra.x[0] = q->ptr;
+    ra.x[1] = k->ptr;
+    for (int a = 0; a < 3; ++a) {
+      ra.xs[0][a] = q->stride[a];
+      ra.xs[1][a] = k->stride[a];
+    }
+    ra.y[0] = workspace;
+    ra.y[1] = static_cast<uint8_t*>(workspace) + one;
+    ra.dtype = dtype;
+    ra.B = B; ra.N = N; ra.H = H; ra.d = static_cast<int32_t>(d);
+    ra.cos_t = rope->cos_t; ra.sin_t = rope->sin_t;
+    ra.cos_h = rope->cos_h; ra.sin_h = rope->sin_h;
+    ra.cos_w = rope->cos_w; ra.sin_w = rope->sin_w;
+    ra.Hl = rope->Hl; ra.Wl = rope->Wl; ra.start_frame = rope->start_frame;
+    ra.dt = rope->dt; ra.dh = rope->dh; ra.dw = rope->dw;
+    if (launch_rope_apply(ra, s) != cudaSuccess) return DITANGO_ERR_CUDA;
+    qp = ra.y[0];
+    kp = ra.y[1];
+    const int64_t cs[4] = {N * H * d, H * d, d, 1};
+    std::memcpy(qs, cs, sizeof(cs));
+    std::memcpy(ks, cs, sizeof(cs));
+  }
+
+  // ---- 2. fresh states of the computed pairs
+  const int32_t block_rows = dtype == DITANGO_BF16 ? 256 : 64;
+  PairSchedule sched;
+  build_schedule(N, static_cast<int32_t>(P), plan->offsets.data(), mask, B, H, block_rows, &sched);
+  if (dtype == DITANGO_BF16) {
+    CUtensorMap mq, mk, mv;
+    const int64_t shp[4] = {B, N, H, d};
+    const int64_t vs[4] = {v->stride[0], v->stride[1], v->stride[2], 1};
+    if (encode_bnhd_map(&mq, qp, shp, qs) != DITANGO_OK ||
+        encode_bnhd_map(&mk, kp, shp, ks) != DITANGO_OK ||
+        encode_bnhd_map(&mv, v->ptr, shp, vs) != DITANGO_OK)
+      return DITANGO_ERR_CUDA;
+    PairTcArgs pa;
+    pa.sched = sched;
+    pa.N = N;
+    pa.cache_O = cO.ptr;
+    pa.cache_lse = static_cast<float*>(cL.ptr);
+    pa.scale_log2 = softmax_scale * 1.4426950408889634f;
+    pa.err = dev->err_ptr;
+    if (launch_pair_tc(static_cast<int>(d), mq, mk, mv, pa, dev->num_sms, s) != cudaSuccess)
+      return DITANGO_ERR_CUDA;
+  } else {
+    PairF32Args pa;
+    pa.sched = sched;
+    pa.N = N;
+    pa.q = static_cast<const float*>(qp);
+    pa.k = static_cast<const float*>(kp);
+    pa.v = static_cast<const float*>(v->ptr);
+    for (int a = 0; a < 3; ++a) {
+      pa.qs[a] = qs[a];
+      pa.ks[a] = ks[a];
+      pa.vs[a] = v->stride[a];
+    }
+    pa.cache_O = static_cast<float*>(cO.ptr);
+    pa.cache_lse = static_cast<float*>(cL.ptr);
+    pa.scale = softmax_scale;
+    if (launch_pair_f32(static_cast<int>(d), pa, s) != cudaSuccess) return DITANGO_ERR_CUDA;
+  }
+
+  // ---- 3. merge every row's P states (cache layout [B, H, P, N, d])
+  MergeArgs ma;
+  std::memset(&ma, 0, sizeof(ma));
+  ma.n = static_cast<int32_t>(P);
+  ma.d = static_cast<int32_t>(d);
+  ma.dtype = dtype;
+  ma.G1 = B; ma.G2 = H; ma.R = N;
+  for (int64_t j = 0; j < P; ++j) {
+    ma.O[j] = static_cast<const uint8_t*>(cO.ptr) + static_cast<size_t>(j * N * d) * elem_size(dtype);
+    ma.lse[j] = static_cast<const float*>(cL.ptr) + j * N;
+  }
+  ma.oS[0] = H * P * N * d; ma.oS[1] = P * N * d; ma.oS[2] = d;
+  ma.lS[0] = H * P * N;     ma.lS[1] = P * N;     ma.lS[2] = 1;
+  ma.out = out->ptr;
+  ma.outS[0] = out->stride[0]; ma.outS[1] = out->stride[2]; ma.outS[2] = out->stride[1];
+  if (out_lse != nullptr) {
+    ma.out_lse = static_cast<float*>(out_lse->ptr);
+    ma.olS[0] = out_lse->stride[0]; ma.olS[1] = out_lse->stride[1]; ma.olS[2] = out_lse->stride[2];
+  }
+  if (launch_merge(ma, s) != cudaSuccess) return DITANGO_ERR_CUDA;
+
+  plan_commit(plan, reuse_mask);
+  return DITANGO_OK;
+}
+
+int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
+                  const ditango_tensor* out_lse, void* stream) {
+  if (sl == nullptr || out == nullptr || out->ptr == nullptr || sl->O == nullptr || sl->lse == nullptr)
+    return DITANGO_ERR_INVALID_ARG;
+  if (sl->n < 1 || sl->n > kMaxStates) return DITANGO_ERR_INVALID_ARG;
+  if (sl->dtype != DITANGO_BF16 && sl->dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  const int64_t G1 = sl->shape[0], G2 = sl->shape[1], R = sl->shape[2], d = sl->shape[3];
+  if (G1 < 0 || G2 < 0 || R < 0 || d < 1) return DITANGO_ERR_SHAPE;
+  const int64_t vec = 16 / static_cast<int64_t>(elem_size(sl->dtype));
+  if (d % vec != 0) return DITANGO_ERR_SHAPE;
+  for (int a = 0; a < 3; ++a)
+    if (sl->O_stride[a] % vec != 0) return DITANGO_ERR_ALIGN;
+  for (int32_t s = 0; s < sl->n; ++s) {
+    if (sl->O[s] == nullptr || sl->lse[s] == nullptr) return DITANGO_ERR_INVALID_ARG;
+    if (!aligned16(sl->O[s])) return DITANGO_ERR_ALIGN;
+  }
+  if (out->dtype != sl->dtype) return DITANGO_ERR_DTYPE;
+  if (out->ndim != 4 || out->shape[0] != G1 || out->shape[1] != G2 || out->shape[2] != R ||
+      out->shape[3] != d || out->stride[3] != 1)
+    return DITANGO_ERR_SHAPE;
+  if (!aligned16(out->ptr)) return DITANGO_ERR_ALIGN;
+  for (int a = 0; a < 3; ++a)
+    if (out->stride[a] % vec != 0) return DITANGO_ERR_ALIGN;
+  if (out_lse != nullptr) {
+    if (out_lse->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+    if (out_lse->dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+    if (out_lse->ndim != 3 || out_lse->shape[0] != G1 || out_lse->shape[1] != G2 ||
+        out_lse->shape[2] != R)
+      return DITANGO_ERR_SHAPE;
+  }
+  MergeArgs ma;
+  std::memset(&ma, 0, sizeof(ma));
+  ma.n = sl->n;
+  ma.d = static_cast<int32_t>(d);
+  ma.dtype = sl->dtype;
+  ma.G1 = G1; ma.G2 = G2; ma.R = R;
+  for (int32_t s = 0; s < sl->n; ++s) {
+    ma.O[s] = sl->O[s];
+    ma.lse[s] = sl->lse[s];
+  }
+  for (int a = 0; a < 3; ++a) {
+    ma.oS[a] = sl->O_stride[a];
+    ma.lS[a] = sl->lse_stride[a];
+    ma.outS[a] = out->stride[a];
+  }
+  if (out_lse != nullptr) {
+    ma.out_lse = static_cast<float*>(out_lse->ptr);
+    for (int a = 0; a < 3; ++a) ma.olS[a] = out_lse->stride[a];
+  }
+  return launch_merge(ma, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DITANGO_OK
+                                                                                  : DITANGO_ERR_CUDA;
+}
+
+int ditango_rope_build_tables(const ditango_rope* rope, double theta, void* stream) {
+  if (rope == nullptr || !(theta > 1.0)) return DITANGO_ERR_INVALID_ARG;
+  if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0 || ((rope->dt | rope->dh | rope->dw) & 1))
+    return DITANGO_ERR_INVALID_ARG;
+  if (rope->T_tab < 0 || rope->Hl < 0 || rope->Wl < 0) return DITANGO_ERR_INVALID_ARG;
+  if ((rope->dt && rope->T_tab && (!rope->cos_t || !rope->sin_t)) ||
+      (rope->dh && rope->Hl && (!rope->cos_h || !rope->sin_h)) ||
+      (rope->dw && rope->Wl && (!rope->cos_w || !rope->sin_w)))
+    return DITANGO_ERR_INVALID_ARG;
+  return launch_rope_tables(*rope, theta, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DITANGO_OK
+             : DITANGO_ERR_CUDA;
+}
+
+int ditango_device_status(void* stream, int32_t* code) {
+  if (code != nullptr) *code = 0;
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != DITANGO_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DITANGO_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->err_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DITANGO_ERR_CUDA;
+  if (v == 0) return DITANGO_OK;
+  const int zero = 0;
+  if (cudaMemcpy(dev->err_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return DITANGO_ERR_CUDA;
+  if (code != nullptr) *code = v;
+  return DITANGO_ERR_DEVICE_TIMEOUT;
+}
+
+const char* ditango_status_string(int status) {
+  switch (status) {
+    case DITANGO_OK: return "ok";
+    case DITANGO_ERR_INVALID_ARG: return "invalid argument";
+    case DITANGO_ERR_INVALID_MASK: return "invalid reuse mask (values must be 0/1, diagonal 0)";
+    case DITANGO_ERR_NO_CACHE: return "reuse of a pair with no cached state";
+    case DITANGO_ERR_SHAPE: return "tensor shape mismatch";
+    case DITANGO_ERR_DTYPE: return "unsupported or mismatched dtype";
+    case DITANGO_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case DITANGO_ERR_WORKSPACE: return "workspace missing or too small";
+    case DITANGO_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case DITANGO_ERR_DEVICE_TIMEOUT: return "a kernel barrier wait timed out";
+    case DITANGO_ERR_UNSUPPORTED: return "unsupported head dimension";
+    default: return "unknown status";
+  }
+}
+
+int ditango_version(void) { return DITANGO_ABI_VERSION; }
+
+}  // extern "C"

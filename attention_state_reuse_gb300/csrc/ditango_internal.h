@@ -1,0 +1,94 @@
+// Internal declarations shared by the host API (api.cu, plan.cpp) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ditango.h"
+
+namespace ditango {
+
+constexpr int kMaxP = DITANGO_MAX_PARTITIONS;
+constexpr int kMaxStates = DITANGO_MAX_STATES;
+
+// Work decomposition of one step for the pair kernels (the mask-driven tile scheduler).
+// A unit is one block of `block_rows` query rows of partition i for one (b, h); a unit
+// visits every KV partition j with bit j of compute_mask[i] set, in ascending j, and emits one
+// state per visited j. Partitions are listed in `order` by decreasing cost (computed KV rows)
+// and units are numbered partition by partition in that order, (b, h) major, query block
+// minor, so that CTAs running side by side share the K/V tiles of one (b, h) through L2.
+struct PairSchedule {
+  int32_t P;
+  int32_t BH;          // B * H
+  int32_t H;
+  int32_t block_rows;  // query rows per unit
+  int32_t n_units;
+  int32_t offsets[kMaxP + 1];
+  uint64_t compute_mask[kMaxP];  // bit j of [i]: pair (i, j) is computed this step
+  int32_t order[kMaxP];          // partition at position k of the unit numbering
+  int32_t seg_start[kMaxP + 1];  // first unit of order[k]; seg_start[P] = n_units
+};
+
+// Fills a schedule. `mask` is P*P (1 = reuse). Host only.
+void build_schedule(int64_t N, int32_t P, const int64_t* offsets, const uint8_t* mask, int64_t B,
+                    int64_t H, int32_t block_rows, PairSchedule* s);
+
+// bf16 pair kernel on tcgen05 (head dim 64 or 128).
+struct PairTcArgs {
+  PairSchedule sched;
+  int64_t N;
+  void* cache_O;      // bf16 [B, H, P, N, d]
+  float* cache_lse;   // [B, H, P, N]
+  float scale_log2;   // softmax scale * log2(e)
+  int* err;           // device error word
+};
+cudaError_t launch_pair_tc(int d, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, const PairTcArgs& args, int num_sms,
+                           cudaStream_t stream);
+
+// fp32 pair kernel on CUDA cores (head dim 64 or 128).
+struct PairF32Args {
+  PairSchedule sched;
+  int64_t N;
+  const float* q; const float* k; const float* v;
+  int64_t qs[3], ks[3], vs[3];  // element strides of b, n, h (d contiguous)
+  float* cache_O;     // [B, H, P, N, d]
+  float* cache_lse;   // [B, H, P, N]
+  float scale;
+};
+cudaError_t launch_pair_f32(int d, const PairF32Args& args, cudaStream_t stream);
+
+// Merge of n states with a common [G1, G2, R, d] layout.
+struct MergeArgs {
+  int32_t n;
+  int32_t d;
+  int32_t dtype;  // of the states and of out
+  int64_t G1, G2, R;
+  const void* O[kMaxStates];
+  const float* lse[kMaxStates];
+  int64_t oS[3], lS[3];
+  void* out;
+  int64_t outS[3];
+  float* out_lse;  // may be null
+  int64_t olS[3];
+};
+cudaError_t launch_merge(const MergeArgs& args, cudaStream_t stream);
+
+// 3D RoPE applied to up to two [B, N, H, d] tensors, written contiguous.
+struct RopeApplyArgs {
+  int32_t n_tensors;
+  const void* x[2];
+  int64_t xs[2][3];  // element strides of b, n, h
+  void* y[2];        // contiguous [B, N, H, d], same dtype as x
+  int32_t dtype;
+  int64_t B, N, H;
+  int32_t d;
+  const float *cos_t, *sin_t, *cos_h, *sin_h, *cos_w, *sin_w;
+  int64_t Hl, Wl, start_frame;
+  int32_t dt, dh, dw;
+};
+cudaError_t launch_rope_apply(const RopeApplyArgs& args, cudaStream_t stream);
+cudaError_t launch_rope_tables(const ditango_rope& rope, double theta, cudaStream_t stream);
+
+}  // namespace ditango

@@ -1,0 +1,434 @@
+// Partition-pair attention states on the sm_103a tensor cores (bf16 in, fp32 accumulate).
+//
+// Method: DiTango (gist.science/paper/2607.15650), Methodology 2, State Composition: for a
+// query partition i and a KV partition j the state is (O_ij, lse_ij) with
+//   lse_ij[r] = ln sum_{c in j} exp(z_c),   O_ij[r] = sum_{c in j} exp(z_c - lse_ij[r]) v_c,
+//   z_c = scale <q_r, k_c>.
+// Only pairs the step computes are visited (Methodology 1: reused pairs launch nothing).
+//
+// Kernel design (persistent, one CTA per SM, 320 threads):
+//   warps 0-3  softmax warpgroup 0: query tile 0 (rows 0..127 of the unit), one row per thread
+//   warps 4-7  softmax warpgroup 1: query tile 1 (rows 128..255)
+//   warp  8    TMA producer: Q tiles per unit, then a ring of K and V tiles (128 rows each)
+//   warp  9    MMA issuer: S_w = Q_w K^T (SS, both K-major) and O_w += P_w V (A from TMEM,
+//              V MN-major); owns the TMEM allocation
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d, 256+2d).
+// P_w overwrites the first 64 columns of S_w as packed bf16; tcgen05.mma operations issued by
+// one thread execute in order, so S_w of the next tile is written only after P_w is consumed.
+// The online softmax keeps a stale running max until the new tile max exceeds it by more than
+// 2^8 (values of P then stay below 256); only then are O and the row sum rescaled.
+// Every barrier wait is bounded (see ptx_sm103.cuh); a timeout makes all roles stop, drain
+// their copies, free TMEM and record an error code.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+
+#include "ditango_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace ditango {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTileRows = 128;               // query rows per tile == KV rows per tile
+constexpr int kUnitRows = 2 * kTileRows;     // query rows per unit
+constexpr int kChunkBytes = 128 * 128;       // 128 rows x 64 bf16 (one swizzle-atom column)
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+template <int D>
+struct Cfg {
+  static constexpr int CH = D / 64;
+  static constexpr int TILE_BYTES = CH * kChunkBytes;
+  static constexpr int Q_BYTES = 2 * TILE_BYTES;
+  static constexpr int STAGES = (D == 128) ? 4 : 8;
+  __host__ __device__ static constexpr uint32_t s_col(int w) { return w ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t o_col(int w) { return 256u + (w ? D : 0); }
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, true);
+};
+
+template <int STAGES>
+struct SharedCtl {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[STAGES], kv_empty[STAGES];
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t drained;
+  uint32_t tmem_base;
+  int abort_word;
+};
+
+template <int D>
+constexpr int smem_bytes() {
+  return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::STAGES * Cfg<D>::TILE_BYTES +
+         (int)sizeof(SharedCtl<Cfg<D>::STAGES>);
+}
+
+struct UnitInfo {
+  int b, h, i, qb, row0, n_i;
+};
+
+__device__ __forceinline__ UnitInfo decode_unit(const PairSchedule& s, int u) {
+  int k = 0;
+  while (u >= s.seg_start[k + 1]) ++k;
+  UnitInfo ui;
+  ui.i = s.order[k];
+  const int local = u - s.seg_start[k];
+  ui.n_i = s.offsets[ui.i + 1] - s.offsets[ui.i];
+  const int blocks = (ui.n_i + s.block_rows - 1) / s.block_rows;
+  const int bh = local / blocks;
+  ui.qb = local - bh * blocks;
+  ui.b = bh / s.H;
+  ui.h = bh - ui.b * s.H;
+  ui.row0 = s.offsets[ui.i] + ui.qb * s.block_rows;
+  return ui;
+}
+
+__device__ __forceinline__ int ntiles_of(const PairSchedule& s, int j) {
+  return (s.offsets[j + 1] - s.offsets[j] + kTileRows - 1) / kTileRows;
+}
+
+// Waits with the CTA's abort word; the result is made uniform across the warp so that
+// warp-collective tcgen05 operations are entered by all lanes or by none.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_w) {
+  const bool ok = mbar_wait(bar, parity, abort_w);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Drain wait: ignores the abort word, bounded by the timeout alone.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  int dummy = 0;
+  (void)mbar_wait(bar, parity, &dummy);
+}
+
+// Issues O_w (+)= P_w V for the tile before the current one: waits for P_w of that tile, for
+// the epilogue of the previous partition to have read O_w (first tile of a partition), and
+// for the V tile; then eight K=16 steps with A read from TMEM (P) and B = V (MN-major).
+template <int D>
+__device__ __forceinline__ bool issue_pv(SharedCtl<Cfg<D>::STAGES>* ctl, int w, uint32_t prev_g,
+                                         uint32_t prev_v, uint32_t prev_pidx, bool prev_first,
+                                         uint32_t kv_addr, uint32_t tbase, volatile int* abort_w) {
+  using C = Cfg<D>;
+  constexpr int STAGES = C::STAGES;
+  if (!mbar_wait(&ctl->p_full[w], prev_g & 1u, abort_w)) return false;
+  if (prev_first && prev_pidx >= 1 && !mbar_wait(&ctl->o_free[w], (prev_pidx - 1) & 1u, abort_w))
+    return false;
+  if (w == 0 && !mbar_wait(&ctl->kv_full[prev_v % STAGES], (prev_v / STAGES) & 1u, abort_w))
+    return false;
+  tc_fence_after_sync();
+  const uint32_t v_addr = kv_addr + (prev_v % STAGES) * C::TILE_BYTES;
+#pragma unroll
+  for (int k = 0; k < kTileRows / 16; ++k) {
+    const uint64_t bdesc = sdesc_sw128(v_addr + k * 2048, kChunkBytes, 1024);
+    mma_bf16_ts(tbase + C::o_col(w), tbase + C::s_col(w) + k * 8, bdesc, C::IDESC_PV,
+                (k > 0 || !prev_first) ? 1u : 0u);
+  }
+  tc_commit(&ctl->o_done[w]);
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    pair_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ PairTcArgs args) {
+  using C = Cfg<D>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_smem = smem;
+  uint8_t* kv_smem = smem + C::Q_BYTES;
+  auto* ctl = reinterpret_cast<SharedCtl<STAGES>*>(kv_smem + STAGES * C::TILE_BYTES);
+  volatile int* abort_w = &ctl->abort_word;
+
+  const PairSchedule& sch = args.sched;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    ctl->abort_word = 0;
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->kv_full[s], 1);
+      mbar_init(&ctl->kv_empty[s], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&ctl->s_full[w], 1);
+      mbar_init(&ctl->p_full[w], kTileRows);
+      mbar_init(&ctl->o_done[w], 1);
+      mbar_init(&ctl->o_free[w], kTileRows);
+    }
+    mbar_init(&ctl->drained, 1);
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_k);
+    tma_prefetch_map(&map_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = ctl->tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t e = 0, uc = 0;  // K/V ring entries and Q loads issued so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x) {
+        const UnitInfo ui = decode_unit(sch, u);
+        if (uc > 0) ok = mbar_wait(&ctl->q_empty, (uc - 1) & 1u, abort_w);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&ctl->q_full, C::Q_BYTES);
+        ++uc;
+        for (int w = 0; w < 2; ++w)
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_4d(q_smem + w * C::TILE_BYTES + c * kChunkBytes, &map_q, &ctl->q_full, c * 64,
+                        ui.h, ui.row0 + w * kTileRows, ui.b);
+        for (uint64_t m = sch.compute_mask[ui.i]; ok && m; m &= m - 1) {
+          const int j = __ffsll(static_cast<long long>(m)) - 1;
+          const int nt = ntiles_of(sch, j);
+          for (int t = 0; ok && t < nt; ++t) {
+            const int kvrow = sch.offsets[j] + t * kTileRows;
+            for (int kind = 0; kind < 2; ++kind, ++e) {
+              const uint32_t slot = e % STAGES;
+              if (e >= static_cast<uint32_t>(STAGES)) {
+                ok = mbar_wait(&ctl->kv_empty[slot], ((e / STAGES) - 1) & 1u, abort_w);
+                if (!ok) break;
+              }
+              mbar_arrive_expect_tx(&ctl->kv_full[slot], C::TILE_BYTES);
+              const CUtensorMap* mp = kind == 0 ? &map_k : &map_v;
+              for (int c = 0; c < C::CH; ++c)
+                tma_load_4d(kv_smem + slot * C::TILE_BYTES + c * kChunkBytes, mp, &ctl->kv_full[slot],
+                            c * 64, ui.h, kvrow, ui.b);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy this thread started land before the CTA can exit
+        if (uc > 0) drain_wait(&ctl->q_full, (uc - 1) & 1u);
+        const uint32_t lo = e > static_cast<uint32_t>(STAGES) ? e - STAGES : 0u;
+        for (uint32_t x = lo; x < e; ++x) drain_wait(&ctl->kv_full[x % STAGES], (x / STAGES) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t e = 0, uc = 0, g = 0, pidx = 0;
+      bool ok = true;
+      const uint32_t q_addr = smem_u32(q_smem);
+      const uint32_t kv_addr = smem_u32(kv_smem);
+      for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x, ++uc) {
+        const UnitInfo ui = decode_unit(sch, u);
+        ok = mbar_wait(&ctl->q_full, uc & 1u, abort_w);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // previous tile (for the P V product that trails each S = Q K^T by one tile)
+        bool have_prev = false, prev_first = false;
+        uint32_t prev_g = 0, prev_v = 0, prev_pidx = 0;
+        for (uint64_t m = sch.compute_mask[ui.i]; ok && m; m &= m - 1) {
+          const int j = __ffsll(static_cast<long long>(m)) - 1;
+          const int nt = ntiles_of(sch, j);
+          for (int t = 0; t < nt; ++t, e += 2, ++g) {
+            const uint32_t ke = e;
+            ok = mbar_wait(&ctl->kv_full[ke % STAGES], (ke / STAGES) & 1u, abort_w);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t k_addr = kv_addr + (ke % STAGES) * C::TILE_BYTES;
+            for (int w = 0; w < 2; ++w) {
+              if (have_prev && !(ok = issue_pv<D>(ctl, w, prev_g, prev_v, prev_pidx, prev_first, kv_addr, tbase, abort_w))) break;
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+                const uint64_t adesc = sdesc_sw128(q_addr + w * C::TILE_BYTES + off, 16, 1024);
+                const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
+                mma_bf16_ss(tbase + C::s_col(w), adesc, bdesc, C::IDESC_QK, k > 0 ? 1u : 0u);
+              }
+              tc_commit(&ctl->s_full[w]);
+            }
+            if (!ok) break;
+            tc_commit(&ctl->kv_empty[ke % STAGES]);
+            if (have_prev) tc_commit(&ctl->kv_empty[prev_v % STAGES]);
+            have_prev = true;
+            prev_first = (t == 0);
+            prev_g = g;
+            prev_v = ke + 1;
+            prev_pidx = pidx;
+          }
+          ++pidx;
+        }
+        if (!ok) break;
+        tc_commit(&ctl->q_empty);  // every Q K^T of this unit has been issued
+        if (!have_prev) continue;  // a unit always visits its own partition; kept for safety
+        for (int w = 0; ok && w < 2; ++w)
+          ok = issue_pv<D>(ctl, w, prev_g, prev_v, prev_pidx, prev_first, kv_addr, tbase, abort_w);
+        if (!ok) break;
+        tc_commit(&ctl->kv_empty[prev_v % STAGES]);
+      }
+      tc_commit(&ctl->drained);
+      drain_wait(&ctl->drained, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int w = warp >> 2;              // query tile of this warpgroup
+    const int lrow = threadIdx.x & 127;   // row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_taddr = tbase + lane_base + C::s_col(w);
+    const uint32_t o_taddr = tbase + lane_base + C::o_col(w);
+    const float sl2 = args.scale_log2;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x) {
+      const UnitInfo ui = decode_unit(sch, u);
+      const int qrow = ui.qb * kUnitRows + w * kTileRows + lrow;  // row within partition i
+      const bool row_ok = qrow < ui.n_i;
+      for (uint64_t m = sch.compute_mask[ui.i]; ok && m; m &= m - 1) {
+        const int j = __ffsll(static_cast<long long>(m)) - 1;
+        const int nj = sch.offsets[j + 1] - sch.offsets[j];
+        const int nt = (nj + kTileRows - 1) / kTileRows;
+        float m_run = -FLT_MAX, l_run = 0.f;
+        for (int t = 0; t < nt; ++t, ++g) {
+          ok = warp_wait(&ctl->s_full[w], g & 1u, abort_w);
+          if (!ok) break;
+          tc_fence_after_sync();
+          float s[kTileRows];
+          {
+            uint32_t r[kTileRows];
+            tmem_ld_32x32b_x128(s_taddr, r);
+#pragma unroll
+            for (int c = 0; c < kTileRows; ++c) s[c] = __uint_as_float(r[c]);
+          }
+          const int valid = nj - t * kTileRows;
+          if (valid < kTileRows) {
+#pragma unroll
+            for (int c = 0; c < kTileRows; ++c)
+              if (c >= valid) s[c] = -INFINITY;
+          }
+          float mx = s[0];
+#pragma unroll
+          for (int c = 1; c < kTileRows; ++c) mx = fmaxf(mx, s[c]);
+          const float m_tile = mx * sl2;
+          bool need_rescale = false;
+          float alpha = 1.f;
+          if (t == 0) {
+            m_run = m_tile;
+            l_run = 0.f;
+          } else if (m_tile > m_run + kRescaleLog2) {
+            alpha = ex2_approx(m_run - m_tile);
+            m_run = m_tile;
+            l_run *= alpha;
+            need_rescale = true;
+          }
+          if (__any_sync(0xffffffffu, need_rescale)) {
+            // O holds the sum over earlier tiles of this partition: wait for the last P V
+            ok = warp_wait(&ctl->o_done[w], (g - 1) & 1u, abort_w);
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(o_taddr + c * 32, r);
+#pragma unroll
+              for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+              tmem_st_32x32b_x32(o_taddr + c * 32, r);
+            }
+          }
+          const float neg_m = -m_run;
+          float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float p0 = ex2_approx(fmaf(s[64 * half + 2 * c], sl2, neg_m));
+              const float p1 = ex2_approx(fmaf(s[64 * half + 2 * c + 1], sl2, neg_m));
+              lsum0 += p0;
+              lsum1 += p1;
+              pk[c] = pack_bf16x2(p0, p1);
+            }
+            tmem_st_32x32b_x32(s_taddr + 32 * half, pk);
+          }
+          l_run += lsum0 + lsum1;
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&ctl->p_full[w]);
+        }
+        if (!ok) break;
+        // ---- epilogue of pair (i, j): O_ij = O / l, lse_ij = ln(l) + max
+        ok = warp_wait(&ctl->o_done[w], (g - 1) & 1u, abort_w);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const float inv_l = 1.f / l_run;
+        const size_t slot = (static_cast<size_t>(ui.b * sch.H + ui.h) * sch.P + j) *
+                                static_cast<size_t>(args.N) +
+                            static_cast<size_t>(ui.row0 + w * kTileRows + lrow);
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.cache_O) + slot * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(o_taddr + c * 32, r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pk[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+        if (row_ok) args.cache_lse[slot] = (m_run + __log2f(l_run)) * kLn2;
+        tc_fence_before_sync();
+        mbar_arrive(&ctl->o_free[w]);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && ctl->abort_word) atomicExch(args.err, 1);
+}
+
+}  // namespace
+
+cudaError_t launch_pair_tc(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const PairTcArgs& args, int num_sms, cudaStream_t stream) {
+  if (args.sched.n_units <= 0) return cudaSuccess;
+  const int grid = args.sched.n_units < num_sms ? args.sched.n_units : num_sms;
+  cudaError_t err;
+  if (d == 128) {
+    constexpr int smem = smem_bytes<128>();
+    err = cudaFuncSetAttribute(pair_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    pair_tc_kernel<128><<<grid, kThreads, smem, stream>>>(mq, mk, mv, args);
+  } else if (d == 64) {
+    constexpr int smem = smem_bytes<64>();
+    err = cudaFuncSetAttribute(pair_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    pair_tc_kernel<64><<<grid, kThreads, smem, stream>>>(mq, mk, mv, args);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ditango

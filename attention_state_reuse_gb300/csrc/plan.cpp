@@ -1,0 +1,173 @@
+// Host planner: contiguous partitions, reuse-mask validation, cache bookkeeping, and the work
+// decomposition (schedule) handed to the pair kernels.
+//
+// Source: DiTango (gist.science/paper/2607.15650), Problem Statement (the sequence is split
+// into context partitions) and Methodology 1, Anchor-Guided Selection Planner (per step each
+// partition pair computes fresh or reuses an earlier state; local states are always computed,
+// so the diagonal of a reuse mask must be 0; a pair can only be reused once a state for it
+// exists, so the first step computes every pair).
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <numeric>
+#include <vector>
+
+#include "ditango_internal.h"
+#include "plan_internal.h"
+
+using ditango::kMaxP;
+
+namespace {
+
+int check_values(int32_t P, const uint8_t* mask) {
+  if (mask == nullptr) return DITANGO_OK;
+  for (int32_t i = 0; i < P; ++i) {
+    for (int32_t j = 0; j < P; ++j) {
+      const uint8_t m = mask[i * P + j];
+      if (m > 1) return DITANGO_ERR_INVALID_MASK;
+      if (i == j && m != 0) return DITANGO_ERR_INVALID_MASK;
+    }
+  }
+  return DITANGO_OK;
+}
+
+}  // namespace
+
+namespace ditango {
+
+const uint8_t* plan_effective_mask(const ditango_plan_s* p, const uint8_t* mask) {
+  return mask != nullptr ? mask : p->mask.data();
+}
+
+int plan_validate(const ditango_plan_s* p, const uint8_t* mask) {
+  const uint8_t* m = plan_effective_mask(p, mask);
+  const int st = check_values(p->P, m);
+  if (st != DITANGO_OK) return st;
+  for (size_t x = 0; x < p->valid.size(); ++x)
+    if (m[x] == 1 && !p->valid[x]) return DITANGO_ERR_NO_CACHE;
+  return DITANGO_OK;
+}
+
+void plan_commit(ditango_plan_s* p, const uint8_t* mask) {
+  const uint8_t* m = plan_effective_mask(p, mask);
+  for (size_t x = 0; x < p->valid.size(); ++x) {
+    if (m[x] == 0) {
+      p->valid[x] = 1;
+      p->step_computed[x] = p->steps;
+    }
+  }
+  ++p->steps;
+}
+
+void build_schedule(int64_t N, int32_t P, const int64_t* offsets, const uint8_t* mask, int64_t B,
+                    int64_t H, int32_t block_rows, PairSchedule* s) {
+  (void)N;
+  std::memset(s, 0, sizeof(*s));
+  s->P = P;
+  s->BH = static_cast<int32_t>(B * H);
+  s->H = static_cast<int32_t>(H);
+  s->block_rows = block_rows;
+  std::vector<int64_t> cost(P, 0);
+  for (int32_t i = 0; i <= P; ++i) s->offsets[i] = static_cast<int32_t>(offsets[i]);
+  for (int32_t i = 0; i < P; ++i) {
+    uint64_t bits = 0;
+    for (int32_t j = 0; j < P; ++j) {
+      if (mask[i * P + j] == 0) {
+        bits |= uint64_t{1} << j;
+        cost[i] += offsets[j + 1] - offsets[j];
+      }
+    }
+    s->compute_mask[i] = bits;
+  }
+  std::vector<int32_t> order(P);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+  int64_t acc = 0;
+  for (int32_t k = 0; k < P; ++k) {
+    const int32_t i = order[k];
+    s->order[k] = i;
+    s->seg_start[k] = static_cast<int32_t>(acc);
+    const int64_t n_i = offsets[i + 1] - offsets[i];
+    acc += ((n_i + block_rows - 1) / block_rows) * B * H;
+  }
+  s->seg_start[P] = static_cast<int32_t>(acc);
+  s->n_units = static_cast<int32_t>(acc);
+}
+
+}  // namespace ditango
+
+extern "C" {
+
+int ditango_plan(int64_t N, int32_t P, const uint8_t* mask, ditango_plan_t* out_plan) {
+  if (out_plan == nullptr || P < 1 || P > kMaxP || N < P || N > (int64_t{1} << 30))
+    return DITANGO_ERR_INVALID_ARG;
+  const int st = check_values(P, mask);
+  if (st != DITANGO_OK) return st;
+  auto* p = new (std::nothrow) ditango_plan_s;
+  if (p == nullptr) return DITANGO_ERR_INVALID_ARG;
+  p->N = N;
+  p->P = P;
+  p->offsets.resize(P + 1);
+  const int64_t base = N / P, extra = N % P;
+  p->offsets[0] = 0;
+  for (int32_t i = 0; i < P; ++i) p->offsets[i + 1] = p->offsets[i] + base + (i < extra ? 1 : 0);
+  p->mask.assign(static_cast<size_t>(P) * P, 0);
+  if (mask != nullptr) std::memcpy(p->mask.data(), mask, p->mask.size());
+  p->valid.assign(static_cast<size_t>(P) * P, 0);
+  p->step_computed.assign(static_cast<size_t>(P) * P, -1);
+  p->steps = 0;
+  *out_plan = p;
+  return DITANGO_OK;
+}
+
+void ditango_plan_destroy(ditango_plan_t plan) { delete plan; }
+
+int ditango_plan_set_mask(ditango_plan_t plan, const uint8_t* mask) {
+  if (plan == nullptr || mask == nullptr) return DITANGO_ERR_INVALID_ARG;
+  const int st = check_values(plan->P, mask);
+  if (st != DITANGO_OK) return st;
+  std::memcpy(plan->mask.data(), mask, plan->mask.size());
+  return DITANGO_OK;
+}
+
+int ditango_plan_check_mask(ditango_plan_t plan, const uint8_t* mask) {
+  if (plan == nullptr) return DITANGO_ERR_INVALID_ARG;
+  return ditango::plan_validate(plan, mask);
+}
+
+int ditango_plan_get_offsets(ditango_plan_t plan, int64_t* offsets) {
+  if (plan == nullptr || offsets == nullptr) return DITANGO_ERR_INVALID_ARG;
+  std::copy(plan->offsets.begin(), plan->offsets.end(), offsets);
+  return DITANGO_OK;
+}
+
+int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pairs,
+                           int32_t* count) {
+  if (plan == nullptr || pairs == nullptr || count == nullptr) return DITANGO_ERR_INVALID_ARG;
+  const int st = check_values(plan->P, mask);
+  if (st != DITANGO_OK) return st;
+  const uint8_t* m = ditango::plan_effective_mask(plan, mask);
+  int32_t n = 0;
+  for (int32_t i = 0; i < plan->P; ++i)
+    for (int32_t j = 0; j < plan->P; ++j)
+      if (m[i * plan->P + j] == 0) {
+        pairs[2 * n] = i;
+        pairs[2 * n + 1] = j;
+        ++n;
+      }
+  *count = n;
+  return DITANGO_OK;
+}
+
+int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* step_computed,
+                                 int64_t* steps_run) {
+  if (plan == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (valid != nullptr) std::copy(plan->valid.begin(), plan->valid.end(), valid);
+  if (step_computed != nullptr)
+    std::copy(plan->step_computed.begin(), plan->step_computed.end(), step_computed);
+  if (steps_run != nullptr) *steps_run = plan->steps;
+  return DITANGO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,212 @@
+/*
+ * ditango.h - C ABI of a single-GPU (GB300, sm_103a) library for partitioned attention with
+ * attention-state reuse, as used for video diffusion-transformer inference.
+ *
+ * Method: "DiTango: Cost-Effective Parallel Diffusion Generation with Selective Attention State
+ * Reuse" (gist.science/paper/2607.15650), Technical Summary, Methodology:
+ *   1. Anchor-Guided Selection Planner - per step, each (query partition i, KV partition j)
+ *      pair either computes a fresh attention state or reuses the state cached at an earlier
+ *      step; anchor steps compute every pair; local states are always computed.
+ *   2. State-Centric Parallel Runtime, State Composition - an attention state is the output
+ *      plus the log-sum-exp; states combine associatively and commutatively, and the composed
+ *      states are what is cached.
+ * Optional rotary prologue: "Accelerating Video Generation Inference with Sequential-Parallel
+ * 3D Positional Encoding Using a Global Time Index" (gist.science/es/paper/2603.06664),
+ * section 2 (t_global = t_local + s; sin/cos precomputed into contiguous tensors).
+ *
+ * Definitions used throughout (the pages print no formula; these are the plain readings):
+ *   partitions   contiguous slices of the N tokens; the first N mod P partitions hold one
+ *                extra row (offsets[p] = p*floor(N/P) + min(p, N mod P)).
+ *   pair state   for query row r and KV partition j, with z_c = scale * <q_r, k_c>:
+ *                lse_ij[r] = ln sum_{c in j} exp(z_c)     (natural log)
+ *                O_ij[r]   = sum_{c in j} exp(z_c - lse_ij[r]) * v_c
+ *                i.e. O is normalised within partition j only.
+ *   merge        lse = ln sum_j exp(lse_j);  O = sum_j exp(lse_j - lse) * O_j.
+ *   reuse mask   P x P bytes, row-major, mask[i*P + j] = 1: reuse the cached state of pair
+ *                (i, j); 0: compute it from this step's inputs. The diagonal must be 0.
+ *
+ * Conventions:
+ *   - Every device buffer is allocated and owned by the caller. No entry point allocates or
+ *     frees device memory.
+ *   - Entry points taking `stream` are asynchronous on that stream (a cudaStream_t passed as
+ *     void*; NULL means the legacy default stream). Host-side validation happens before any
+ *     launch; on any error nothing is launched and no plan state changes.
+ *   - Return value: a ditango_status (0 = success). No C++ exception crosses this boundary.
+ *   - Thread safety: a plan must not be used from two threads at once.
+ */
+#ifndef DITANGO_H_
+#define DITANGO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DITANGO_ABI_VERSION 1
+#define DITANGO_MAX_PARTITIONS 64 /* P limit of a plan */
+#define DITANGO_MAX_STATES 64     /* state limit of one ditango_merge call */
+
+typedef enum {
+  DITANGO_OK = 0,
+  DITANGO_ERR_INVALID_ARG = 1,     /* null pointer, N < P, P outside [1, 64], ... */
+  DITANGO_ERR_INVALID_MASK = 2,    /* a value other than 0/1, or a reused diagonal pair */
+  DITANGO_ERR_NO_CACHE = 3,        /* the mask reuses a pair never computed under this plan */
+  DITANGO_ERR_SHAPE = 4,           /* tensor shapes disagree with the plan or each other */
+  DITANGO_ERR_DTYPE = 5,           /* unsupported or mismatched element type */
+  DITANGO_ERR_ALIGN = 6,           /* pointer or stride not 16-byte aligned where required */
+  DITANGO_ERR_WORKSPACE = 7,       /* workspace missing or smaller than required */
+  DITANGO_ERR_CUDA = 8,            /* a CUDA runtime/driver call or a kernel launch failed */
+  DITANGO_ERR_DEVICE_TIMEOUT = 9,  /* a kernel gave up waiting on one of its own barriers */
+  DITANGO_ERR_UNSUPPORTED = 10     /* head dim / dtype combination not built */
+} ditango_status;
+
+typedef enum { DITANGO_F32 = 0, DITANGO_BF16 = 1 } ditango_dtype;
+
+/* A strided view of device memory. `stride` is in elements. Unused trailing dims ignored. */
+typedef struct {
+  void* ptr;
+  int32_t dtype; /* ditango_dtype */
+  int32_t ndim;
+  int64_t shape[5];
+  int64_t stride[5];
+} ditango_tensor;
+
+/* The state cache of one attention layer, owned by the caller and passed unchanged every
+ * step. O: [B, H, P, N, d], contiguous, dtype BF16 for bf16 inputs and F32 for f32 inputs.
+ * lse: [B, H, P, N], contiguous, F32. Slot [b, h, j, r] holds the state of (partition(r), j)
+ * for query row r. Contents are meaningful only for pairs this plan has computed. */
+typedef struct {
+  ditango_tensor O;
+  ditango_tensor lse;
+} ditango_state_cache;
+
+/* Precomputed 3D RoPE tables (device memory, fp32, row-major, filled by
+ * ditango_rope_build_tables). Channel pairs (2m, 2m+1) of each head: the first dt/2 pairs turn
+ * with the global frame index t, the next dh/2 with the row h, the last dw/2 with the column w;
+ * pair k of an axis of width d_a turns by pos * theta^(-2k/d_a).
+ * Token n of the sequence sits at t = n / (Hl*Wl) + start_frame, h = (n / Wl) % Hl,
+ * w = n % Wl, so N must be a multiple of Hl*Wl and start_frame + N/(Hl*Wl) <= T_tab. */
+typedef struct {
+  float* cos_t; float* sin_t; /* [T_tab, dt/2] */
+  float* cos_h; float* sin_h; /* [Hl, dh/2] */
+  float* cos_w; float* sin_w; /* [Wl, dw/2] */
+  int64_t T_tab, Hl, Wl;
+  int32_t dt, dh, dw;       /* even, dt + dh + dw = d */
+  int64_t start_frame;      /* s: global frame index of this sequence's first frame */
+} ditango_rope;
+
+/* A list of n states with a common layout, for ditango_merge. State s has outputs O[s]
+ * ([G1, G2, R, d], strides O_stride for G1, G2, R; d contiguous) and log-sum-exps lse[s]
+ * ([G1, G2, R] fp32, strides lse_stride). O and lse are HOST arrays of n DEVICE pointers. */
+typedef struct {
+  int32_t n;     /* 1 .. DITANGO_MAX_STATES */
+  int32_t dtype; /* of every O[s]: F32 or BF16 */
+  const void* const* O;
+  const float* const* lse;
+  int64_t shape[4];      /* G1, G2, R, d */
+  int64_t O_stride[3];   /* elements */
+  int64_t lse_stride[3]; /* elements */
+} ditango_state_list;
+
+typedef struct ditango_plan_s* ditango_plan_t;
+
+/* ---- plan (host only) -------------------------------------------------------------------
+ * Source: DiTango, Methodology 1 (per-step compute/reuse decision per partition pair) and the
+ * partitioning of the sequence into contiguous context partitions (Problem Statement).
+ * Creates a plan for N tokens in P partitions (1 <= P <= 64, N >= P). `mask` (P*P bytes, may
+ * be NULL = every pair computed) becomes the plan's default reuse mask; it is validated for
+ * values and diagonal only (cache validity is checked per step). The plan also holds the
+ * cache bookkeeping: per pair, whether a state has been computed and at which step.
+ * Errors: INVALID_ARG, INVALID_MASK. *out_plan is set only on success. */
+int ditango_plan(int64_t N, int32_t P, const uint8_t* mask, ditango_plan_t* out_plan);
+
+/* Frees the plan (host memory only). NULL is accepted. */
+void ditango_plan_destroy(ditango_plan_t plan);
+
+/* Replaces the default reuse mask (same validation as ditango_plan). */
+int ditango_plan_set_mask(ditango_plan_t plan, const uint8_t* mask);
+
+/* Checks `mask` (NULL = default mask) against the bookkeeping without changing anything:
+ * INVALID_MASK for bad values / reused diagonal, NO_CACHE for reuse of a never-computed pair. */
+int ditango_plan_check_mask(ditango_plan_t plan, const uint8_t* mask);
+
+/* Copies the P+1 partition offsets into `offsets` (host). */
+int ditango_plan_get_offsets(ditango_plan_t plan, int64_t* offsets);
+
+/* Writes the pairs computed under `mask` (NULL = default mask), row-major (i ascending, then
+ * j ascending), as (i, j) int32 pairs into `pairs` (host, room for 2*P*P) and their number
+ * into *count. */
+int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pairs,
+                           int32_t* count);
+
+/* Copies the cache bookkeeping: valid[i*P+j] (1 = a state exists), step_computed[i*P+j]
+ * (-1 = never) and the number of steps run so far. Any output pointer may be NULL. */
+int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* step_computed,
+                                 int64_t* steps_run);
+
+/* ---- one attention-layer step -----------------------------------------------------------
+ * Source: DiTango, Methodology 1-2 (compute or reuse per pair, then compose the states);
+ * rotary prologue from the Causal-RoPE SP page, section 2.
+ * q, k, v: [B, N, H, d] device tensors of one dtype (BF16 or F32), d contiguous; for BF16 the
+ *   other strides must be multiples of 8 elements and the pointers 16-byte aligned.
+ *   Supported d: 64 and 128.
+ * rope: NULL = no rotation; else q and k are rotated (in fp32, rounded to the input dtype)
+ *   before attention; v is never rotated.
+ * reuse_mask: host P*P bytes; NULL = the plan's default mask.
+ * cache: the layer's state cache (see ditango_state_cache). Pairs with mask 0 are computed
+ *   from this step's inputs and overwrite their slots; pairs with mask 1 are read as cached.
+ * out: [B, N, H, d], same dtype as q, d contiguous. out_lse: [B, H, N] F32, or NULL.
+ * softmax_scale: the `scale` of the pair-state definition (commonly 1/sqrt(d)).
+ * workspace: device memory of at least ditango_attn_step_workspace_size(...) bytes, 256-byte
+ *   aligned (may be NULL when that size is 0). Its contents need not be preserved.
+ * On success the computed pairs are recorded in the plan as valid at this step. The result
+ * is complete when the stream reaches this point. Kernel-side barrier timeouts are reported
+ * by ditango_device_status, not here. */
+int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditango_tensor* k,
+                      const ditango_tensor* v, const ditango_rope* rope,
+                      const uint8_t* reuse_mask, const ditango_state_cache* cache,
+                      const ditango_tensor* out, const ditango_tensor* out_lse,
+                      float softmax_scale, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Bytes of workspace ditango_attn_step needs for these shapes (0 without RoPE). */
+size_t ditango_attn_step_workspace_size(ditango_plan_t plan, int64_t B, int64_t H, int32_t d,
+                                        int32_t dtype, int32_t use_rope);
+
+/* ---- state merge -------------------------------------------------------------------------
+ * Source: DiTango, Methodology 2, State Composition and Dynamic Group Compose (cached states
+ * merge into coarser groups without recomputation; the result is itself a state).
+ * Merges the n states of `states` row by row into out ([G1, G2, R, d], same dtype as the
+ * states, d contiguous, strides free) and out_lse ([G1, G2, R] F32, or NULL). Reads only the
+ * listed states. Errors: INVALID_ARG, SHAPE, DTYPE, ALIGN (O pointers / row strides of BF16
+ * states must allow 16-byte vector access), CUDA. */
+int ditango_merge(const ditango_state_list* states, const ditango_tensor* out,
+                  const ditango_tensor* out_lse, void* stream);
+
+/* ---- RoPE tables -------------------------------------------------------------------------
+ * Source: Causal-RoPE SP page, section 2 (frequencies precomputed into contiguous tensors, so
+ * inference moves no positional data between host and GPU). Fills the six fp32 tables of
+ * `rope` (caller-allocated device buffers of the sizes given there) on the device:
+ * cos/sin(pos * theta^(-2k/d_a)) computed in fp64 and rounded to fp32. */
+int ditango_rope_build_tables(const ditango_rope* rope, double theta, void* stream);
+
+/* ---- diagnostics --------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then reports and clears the device-side error word that kernels set
+ * when a bounded barrier wait gives up: DITANGO_OK or DITANGO_ERR_DEVICE_TIMEOUT (with the
+ * kernel's code in *code if code != NULL), or DITANGO_ERR_CUDA. */
+int ditango_device_status(void* stream, int32_t* code);
+
+/* Static description of a status code. */
+const char* ditango_status_string(int status);
+
+/* DITANGO_ABI_VERSION of the loaded library. */
+int ditango_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DITANGO_H_ */

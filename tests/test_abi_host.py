@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+* the shared library loads and exports every entry point declared in include/ditango.h;
+* the planner's partition offsets and computed-pair lists equal the oracle's, bit for bit;
+* masks the method cannot honour are refused with the documented status codes, exactly where
+  the oracle's bookkeeping refuses them (DiTango, Methodology 1: local states are always
+  computed; a pair is reusable only after a state for it exists).
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from attention_state_reuse_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ditango():
+    import attention_state_reuse_gb300 as m
+
+    m.build()
+    m.load_library()
+    return m
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "ditango.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ditango_[a-z_]+)\s*\(", text)))
+
+
+def test_header_symbols_listed_in_binding(ditango):
+    assert header_symbols() == sorted(ditango.SYMBOLS)
+
+
+def test_library_exports_every_header_symbol(ditango):
+    lib = ditango.load_library()
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(ditango):
+    lib = ditango.load_library()
+    assert lib.ditango_version() == 1
+    for code in range(11):
+        assert lib.ditango_status_string(code)
+    assert lib.ditango_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("N,P", [(1024, 4), (4096, 8), (32760, 8), (75600, 16), (32760, 16),
+                                 (32760, 4), (1560, 8), (64, 64), (65, 64), (300, 1), (7, 3)])
+def test_offsets_bit_exact(ditango, N, P):
+    plan = ditango.Plan(N, P)
+    np.testing.assert_array_equal(plan.offsets(), oracle.partition_offsets(N, P))
+
+
+@pytest.mark.parametrize("P", [1, 4, 8, 16, 64])
+def test_pairs_bit_exact(ditango, P):
+    plan = ditango.Plan(max(P, 100), P)
+    book = oracle.ReuseBook(P)
+    masks = [np.zeros((P, P), np.uint8)] + [wl.distance_mask(P, D) for D in range(1, P + 1)]
+    masks.append(wl.random_mask(P, 123))
+    for m in masks:
+        assert plan.pairs(m) == book.computed_pairs(m)
+    assert plan.pairs() == [(i, j) for i in range(P) for j in range(P)]
+
+
+def test_plan_rejects_bad_arguments(ditango):
+    with pytest.raises(ditango.DitangoError) as e:
+        ditango.Plan(3, 4)  # N < P
+    assert e.value.name == "INVALID_ARG"
+    with pytest.raises(ditango.DitangoError):
+        ditango.Plan(100, 0)
+    with pytest.raises(ditango.DitangoError):
+        ditango.Plan(1000, 65)
+    diag = np.zeros((4, 4), np.uint8)
+    diag[2, 2] = 1
+    with pytest.raises(ditango.DitangoError) as e:
+        ditango.Plan(100, 4, diag)
+    assert e.value.name == "INVALID_MASK"
+
+
+def test_mask_checks_match_oracle_book(ditango):
+    P = 8
+    plan = ditango.Plan(4096, P)
+    book = oracle.ReuseBook(P)
+    bad_val = np.zeros((P, P), np.uint8)
+    bad_val[0, 3] = 2
+    diag = np.zeros((P, P), np.uint8)
+    diag[5, 5] = 1
+    cases = [(np.zeros((P, P), np.uint8), 0), (wl.distance_mask(P, 2), 3), (bad_val, 2),
+             (diag, 2), (wl.random_mask(P, 9), 3)]
+    for m, status in cases:
+        assert plan.check_mask(m) == status
+        if status == 0:
+            book.check(m)
+        else:
+            with pytest.raises(oracle.MaskError):
+                book.check(m)
+    # default mask (all computed) is always usable; nothing was run, so nothing is valid
+    assert plan.check_mask(None) == 0
+    valid, sc, steps = plan.cache_state()
+    assert steps == 0 and not valid.any() and (sc == -1).all()
+
+
+def test_workload_mask_fractions():
+    # distance-threshold masks of the configurations (fractions of reused pairs)
+    assert wl.reuse_fraction(wl.distance_mask(4, 2)) == 6 / 16
+    assert wl.reuse_fraction(wl.distance_mask(8, 2)) == 42 / 64
+    assert wl.reuse_fraction(wl.distance_mask(16, 3)) == 182 / 256
+    assert wl.reuse_fraction(wl.distance_mask(8, 1)) == 56 / 64
+    assert wl.reuse_fraction(wl.distance_mask(16, 2)) == 210 / 256
+    m = wl.random_mask(16, 4023)
+    assert (np.diag(m) == 0).all()
+    np.testing.assert_array_equal(m, wl.random_mask(16, 4023))
+    assert 0.3 < wl.reuse_fraction(m) < 0.6

@@ -1,0 +1,188 @@
+"""GPU parity: the library (through its C ABI) against the CPU oracle on the same seeded inputs.
+
+Small sizes compare every row; full sizes compare sampled rows (partition edges, tile edges,
+random rows) of a few heads, in the same launch configuration the benchmark times.
+See tests/gpu_harness.py for what each step checks and the tolerances.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_state_reuse_gb300 as dt
+from attention_state_reuse_gb300 import workloads as wl
+from gpu_harness import ParityRun, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    dt.build()
+    dt.load_library()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+
+
+def run_all_steps(pr, steps=None):
+    errs = []
+    for t in range(pr.w.steps if steps is None else steps):
+        e = pr.step()
+        errs.append(e)
+        assert e["ok"], f"step {t}: {e}"
+    return errs
+
+
+def test_tiny_fp32_all_rows():
+    run_all_steps(ParityRun(wl.get("tiny_fp32")))
+
+
+def test_small_bf16_all_rows_ten_steps():
+    run_all_steps(ParityRun(wl.get("small_bf16")))
+
+
+def test_wan_like_reduced_rope_all_rows():
+    # 3 frames of a 20x26 latent (N = 1560, partitions of 195 rows: two tiles, ragged),
+    # start frame 5 (global time index), per-head scales, d = 128
+    w = wl.scaled(wl.get("wan14b_layer"), "wan_reduced", H=4, T=3, Hl=20, Wl=26, start_frame=5)
+    run_all_steps(ParityRun(w))
+
+
+def test_long_720p_like_reduced_all_rows():
+    w = wl.scaled(wl.get("long_720p"), "long_reduced", H=2, T=3, Hl=15, Wl=16, steps=5)
+    run_all_steps(ParityRun(w))
+
+
+@pytest.mark.parametrize("P,N,d", [(1, 300, 128), (1, 700, 64), (64, 64 * 3 + 5, 128),
+                                   (64, 64, 64), (3, 129, 128), (5, 1000, 64)])
+def test_edge_partitions(P, N, d):
+    # one partition (dense attention), one- to four-row partitions, one row past a tile
+    w = wl.Workload(f"edge_P{P}_N{N}", 9, 1, 3, d, 1, 1, N, P, "bf16", 3, 0.05,
+                    schedule=[("all",), ("dist", 2), ("random",)])
+    pr = ParityRun(w)
+    for t in range(3):
+        e = pr.step(wl.step_mask(w, t) if P > 1 else np.zeros((1, 1), np.uint8))
+        assert e["ok"], f"step {t}: {e}"
+
+
+def test_batch_two_strided_inputs():
+    # B = 2, with q, k, v and out as strided views (each token row padded by 3 spare heads)
+    w = wl.Workload("batch2", 10, 2, 3, 64, 2, 10, 20, 4, "bf16", 2, 0.05,
+                    schedule=[("all",), ("dist", 2)])
+    pr = ParityRun(w, strided=True)
+    assert not pr.out.is_contiguous()
+    run_all_steps(pr)
+
+
+def test_diagonal_only_mask_max_reuse():
+    w = wl.Workload("diag_only", 11, 1, 2, 128, 2, 16, 20, 8, "bf16", 3, 0.05,
+                    schedule=[("all",), ("dist", 1), ("dist", 1)])
+    run_all_steps(ParityRun(w))
+
+
+# ------------------------------------------------------------------- full sizes, sampled rows
+@pytest.mark.parametrize("name,steps,heads", [("wan14b_layer", 2, [0, 17, 39]),
+                                              ("long_720p", 2, [0, 39]),
+                                              ("sweep_P16", 2, [5, 22])])
+def test_full_size_sampled(name, steps, heads):
+    w = wl.get(name)
+    if name == "sweep_P16":
+        w.schedule = [("all",), ("random",)]
+    rows = sample_rows(w, range(len(heads)))
+    pr = ParityRun(w, heads=heads, rows=rows)
+    run_all_steps(pr, steps)
+
+
+# ------------------------------------------------------------------- merge entry point
+@pytest.mark.parametrize("dtype,n,d", [(torch.bfloat16, 1, 128), (torch.bfloat16, 7, 64),
+                                       (torch.bfloat16, 64, 128), (torch.float32, 5, 64),
+                                       (torch.float32, 16, 128)])
+def test_merge_entry_point(dtype, n, d):
+    import oracle
+
+    g = torch.Generator().manual_seed(n * 1000 + d)
+    G1, G2, R = 2, 3, 37
+    O = [torch.randn(G1, G2, R, d, generator=g).to(dtype) for _ in range(n)]
+    L = [torch.randn(G1, G2, R, generator=g) * 4 for _ in range(n)]
+    out = torch.empty(G1, G2, R, d, dtype=dtype, device="cuda")
+    out_lse = torch.empty(G1, G2, R, device="cuda")
+    dt.merge([o.cuda() for o in O], [x.cuda() for x in L], out, out_lse)
+    torch.cuda.synchronize()
+    Os = np.stack([o.float().numpy() for o in O], axis=-2).reshape(-1, n, d)
+    Ls = np.stack([x.numpy() for x in L], axis=-1).reshape(-1, n)
+    ref = [oracle.merge(Os[r], Ls[r]) for r in range(Os.shape[0])]
+    ref_O = np.stack([x[0] for x in ref]).reshape(G1, G2, R, d)
+    ref_L = np.array([x[1] for x in ref]).reshape(G1, G2, R)
+    tol_o, tol_l = (2e-2, 1e-3) if dtype == torch.bfloat16 else (1e-4, 1e-4)
+    if dtype == torch.bfloat16:
+        ref_O = oracle.round_bf16(ref_O)
+    assert np.abs(out.float().cpu().numpy() - ref_O).max() <= tol_o
+    assert np.abs(out_lse.cpu().numpy() - ref_L).max() <= tol_l
+
+
+def test_merge_grouped_equals_flat():
+    # Dynamic Group Compose: merging two group states equals merging all states at once
+    g = torch.Generator().manual_seed(5)
+    n, d, shape = 6, 64, (1, 2, 50)
+    O = [torch.randn(*shape, d, generator=g).cuda() for _ in range(n)]
+    L = [torch.randn(*shape, generator=g).cuda() * 3 for _ in range(n)]
+    flat, flat_l = torch.empty_like(O[0]), torch.empty_like(L[0])
+    dt.merge(O, L, flat, flat_l)
+    ga, ga_l, gb, gb_l = (torch.empty_like(O[0]), torch.empty_like(L[0]),
+                          torch.empty_like(O[0]), torch.empty_like(L[0]))
+    dt.merge(O[:2], L[:2], ga, ga_l)
+    dt.merge(O[2:], L[2:], gb, gb_l)
+    two, two_l = torch.empty_like(O[0]), torch.empty_like(L[0])
+    dt.merge([ga, gb], [ga_l, gb_l], two, two_l)
+    torch.cuda.synchronize()
+    assert (two - flat).abs().max().item() <= 1e-5
+    assert (two_l - flat_l).abs().max().item() <= 1e-5
+
+
+# ------------------------------------------------------------------- host-detected errors
+def _small_setup(dtype=torch.bfloat16, d=64, N=256, P=4, H=2):
+    q = torch.randn(1, N, H, d, device="cuda").to(dtype)
+    cO, cL = dt.new_state_cache(1, H, P, N, d, dtype)
+    out = torch.empty_like(q)
+    return dt.Plan(N, P), q, cO, cL, out
+
+
+def _status(fn):
+    try:
+        fn()
+    except dt.DitangoError as e:
+        return e.name
+    return "OK"
+
+
+def test_error_no_cache_and_invalid_mask():
+    plan, q, cO, cL, out = _small_setup()
+    m = wl.distance_mask(4, 2)
+    assert _status(lambda: dt.attn_step(plan, q, q, q, cO, cL, out, reuse_mask=m)) == "NO_CACHE"
+    diag = np.zeros((4, 4), np.uint8)
+    diag[1, 1] = 1
+    assert _status(lambda: dt.attn_step(plan, q, q, q, cO, cL, out, reuse_mask=diag)) == "INVALID_MASK"
+    # nothing ran: the bookkeeping is untouched
+    assert plan.cache_state()[2] == 0
+    dt.attn_step(plan, q, q, q, cO, cL, out)
+    dt.attn_step(plan, q, q, q, cO, cL, out, reuse_mask=m)
+    torch.cuda.synchronize()
+    assert plan.cache_state()[2] == 2
+
+
+def test_error_shapes_dtypes_alignment_workspace():
+    plan, q, cO, cL, out = _small_setup()
+    bad_N = torch.randn(1, 255, 2, 64, device="cuda").to(torch.bfloat16)
+    assert _status(lambda: dt.attn_step(plan, bad_N, bad_N, bad_N, cO, cL, out)) == "SHAPE"
+    qf = q.float()
+    assert _status(lambda: dt.attn_step(plan, qf, q, q, cO, cL, out)) == "DTYPE"
+    big = torch.randn(1, 256 * 2 * 64 + 1, device="cuda").to(torch.bfloat16)
+    mis = big[0, 1:].view(1, 256, 2, 64)  # 2-byte offset from a 16-byte boundary
+    assert _status(lambda: dt.attn_step(plan, mis, q, q, cO, cL, out)) == "ALIGN"
+    q96 = torch.randn(1, 256, 2, 96, device="cuda").to(torch.bfloat16)
+    c96 = dt.new_state_cache(1, 2, 4, 256, 96, torch.bfloat16)
+    assert _status(lambda: dt.attn_step(plan, q96, q96, q96, *c96, torch.empty_like(q96))) == "UNSUPPORTED"
+    rope = dt.RopeTables(4, 8, 8, 22, 20, 22)
+    small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    assert _status(lambda: dt.attn_step(plan, q, q, q, cO, cL, out, rope=rope,
+                                        workspace=small_ws)) in ("WORKSPACE", "SHAPE")
+    assert plan.cache_state()[2] == 0
