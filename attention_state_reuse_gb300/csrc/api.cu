@@ -190,6 +190,11 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != DITANGO_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto mark = [&](int x) -> bool {
+    return !plan->profile ||
+           cudaEventRecord(static_cast<cudaEvent_t>(plan->events[x]), s) == cudaSuccess;
+  };
+  if (!mark(0)) return DITANGO_ERR_CUDA;
 
   // ---- 1. rotary prologue into the workspace
   const void* qp = q->ptr;
@@ -225,6 +230,7 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   }
 
   // ---- 2. fresh states of the computed pairs
+  if (!mark(1)) return DITANGO_ERR_CUDA;
   const int32_t block_rows = dtype == DITANGO_BF16 ? 256 : 64;
   PairSchedule sched;
   build_schedule(N, static_cast<int32_t>(P), plan->offsets.data(), mask, B, H, block_rows, &sched);
@@ -264,6 +270,7 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   }
 
   // ---- 3. merge every row's P states (cache layout [B, H, P, N, d])
+  if (!mark(2)) return DITANGO_ERR_CUDA;
   MergeArgs ma;
   std::memset(&ma, 0, sizeof(ma));
   ma.n = static_cast<int32_t>(P);
@@ -283,6 +290,7 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     ma.olS[0] = out_lse->stride[0]; ma.olS[1] = out_lse->stride[1]; ma.olS[2] = out_lse->stride[2];
   }
   if (launch_merge(ma, s) != cudaSuccess) return DITANGO_ERR_CUDA;
+  if (!mark(3)) return DITANGO_ERR_CUDA;
 
   plan_commit(plan, reuse_mask);
   return DITANGO_OK;
@@ -324,6 +332,7 @@ int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
   ma.d = static_cast<int32_t>(d);
   ma.dtype = sl->dtype;
   ma.G1 = G1; ma.G2 = G2; ma.R = R;
+  ma.out = out->ptr;
   for (int32_t s = 0; s < sl->n; ++s) {
     ma.O[s] = sl->O[s];
     ma.lse[s] = sl->lse[s];

@@ -160,6 +160,20 @@ int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pa
   return DITANGO_OK;
 }
 
+int ditango_plan_set_profile_events(ditango_plan_t plan, void* const* events) {
+  if (plan == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (events == nullptr) {
+    plan->profile = false;
+    for (auto& e : plan->events) e = nullptr;
+    return DITANGO_OK;
+  }
+  for (int x = 0; x < 4; ++x)
+    if (events[x] == nullptr) return DITANGO_ERR_INVALID_ARG;
+  for (int x = 0; x < 4; ++x) plan->events[x] = events[x];
+  plan->profile = true;
+  return DITANGO_OK;
+}
+
 int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* step_computed,
                                  int64_t* steps_run) {
   if (plan == nullptr) return DITANGO_ERR_INVALID_ARG;

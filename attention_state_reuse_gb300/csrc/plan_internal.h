@@ -13,6 +13,8 @@ struct ditango_plan_s {
   std::vector<uint8_t> valid;         // a state exists for pair (i, j)
   std::vector<int64_t> step_computed; // step at which pair (i, j) was last computed, -1 never
   int64_t steps = 0;                  // steps run so far
+  void* events[4] = {nullptr, nullptr, nullptr, nullptr};  // optional timing hook
+  bool profile = false;
 };
 
 namespace ditango {

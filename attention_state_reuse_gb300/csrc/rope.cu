@@ -13,7 +13,9 @@
 // Token n sits at t = n / (Hl Wl) + s, h = (n / Wl) mod Hl, w = n mod Wl.
 //
 // rope_apply_kernel: memory bound; one thread rotates 8 channels (4 pairs) of one (b, n, h),
-// reading 16 bytes and writing 16 bytes (bf16), the rotation itself in fp32.
+// reading 16 bytes and writing 16 bytes (bf16). The rotation is evaluated in fp32 as
+// y0 = fl(fl(x0 c) - fl(x1 s)), y1 = fl(fl(x0 s) + fl(x1 c)) with fp32 tables c, s, then
+// rounded (nearest-even) to the storage dtype.
 #include <cuda_bf16.h>
 
 #include "ditango_internal.h"
@@ -83,8 +85,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(const __grid_c
       const int m = grp * kPairsPerThread + p;
       float cs, sn;
       pair_table(a, m, t, hh, ww, cs, sn);
-      y[2 * p] = x[2 * p] * cs - x[2 * p + 1] * sn;
-      y[2 * p + 1] = x[2 * p] * sn + x[2 * p + 1] * cs;
+      // explicit round-to-nearest products and sums (never contracted into FMA), so that the
+      // rotated value rounded to the storage dtype is a reproducible fp32 result
+      y[2 * p] = __fsub_rn(__fmul_rn(x[2 * p], cs), __fmul_rn(x[2 * p + 1], sn));
+      y[2 * p + 1] = __fadd_rn(__fmul_rn(x[2 * p], sn), __fmul_rn(x[2 * p + 1], cs));
     }
     if constexpr (sizeof(T) == 2) {
       uint32_t wv[4];

@@ -146,6 +146,13 @@ int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pa
 int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* step_computed,
                                  int64_t* steps_run);
 
+/* Optional timing hook. `events` is a host array of 4 cudaEvent_t handles (created by the
+ * caller, passed as void*), or NULL to switch the hook off. While set, every
+ * ditango_attn_step on this plan records events[0] before the rotary prologue, events[1]
+ * before the pair kernel, events[2] before the merge and events[3] after it, on the step's
+ * stream, so that the caller can read per-kernel device time with cudaEventElapsedTime. */
+int ditango_plan_set_profile_events(ditango_plan_t plan, void* const* events);
+
 /* ---- one attention-layer step -----------------------------------------------------------
  * Source: DiTango, Methodology 1-2 (compute or reuse per pair, then compose the states);
  * rotary prologue from the Causal-RoPE SP page, section 2.

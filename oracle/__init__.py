@@ -35,11 +35,13 @@ ROUND_NONE, ROUND_BF16, ROUND_F32 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
-    """Compile the C oracle in place (gcc, -O2, IEEE arithmetic, no host-specific flags)."""
+    """Compile the C oracle in place (gcc -O2, IEEE arithmetic without FMA contraction, no
+    host-specific flags, so x86-64 and aarch64 builds give the same results)."""
     if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o",
+           tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -61,7 +63,8 @@ def _load():
         lib.oracle_round_array.argtypes = [dp, i64, i32]
         lib.oracle_rope_rotate.argtypes = [dp, dp, i32, i32, i32, i32, i64, i64, i64, dbl]
         lib.oracle_rope_apply.argtypes = [dp, dp, i64, i64, i64, i32, i32, i32, i32, i64, i64,
-                                          i64, dbl, i32, i32]
+                                          i64, dbl, i32, i32, i32]
+        lib.oracle_rope_rotate_f32.argtypes = [dp, dp, i32, i32, i32, i32, i64, i64, i64, dbl]
         lib.oracle_pair_state.argtypes = [dp, dp, dp, i64, i64, i64, i32, dbl, dp, dp, dp]
         lib.oracle_merge.argtypes = [dp, dp, i32, i32, dp, dp]
         lib.oracle_rows_step.argtypes = [dp, dp, dp, i64, i64, i64, i32, i32, i64p, u8p, dbl,
@@ -118,15 +121,27 @@ def rope_rotate(x: np.ndarray, t: int, h: int, w: int, dt: int, dh: int, dw: int
     return y
 
 
+def rope_rotate_f32(x: np.ndarray, t: int, h: int, w: int, dt: int, dh: int, dw: int,
+                    theta: float = 10000.0) -> np.ndarray:
+    """Rotate one d-vector with the rotation evaluated in fp32 (fp32 cos/sin, no FMA)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().oracle_rope_rotate_f32(_dp(x), _dp(y), x.size, dt, dh, dw, t, h, w, theta)
+    return y
+
+
 def rope_apply(x: np.ndarray, Hl: int, Wl: int, start_frame: int, dt: int, dh: int, dw: int,
-               theta: float = 10000.0, round_mode: int = ROUND_NONE,
+               theta: float = 10000.0, round_mode: int = ROUND_NONE, f32_eval: bool = False,
                nthreads: int | None = None) -> np.ndarray:
-    """Rotate a [B, N, H, d] tensor by the 3D RoPE of each token's (t_global, h, w)."""
+    """Rotate a [B, N, H, d] tensor by the 3D RoPE of each token's (t_global, h, w).
+
+    round_mode rounds the result to bf16 / fp32; with f32_eval the rotation is evaluated in
+    fp32 first (the precision in which a kernel takes that rounding decision)."""
     x = np.ascontiguousarray(x, dtype=np.float64)
     B, N, H, d = x.shape
     y = np.empty_like(x)
     _load().oracle_rope_apply(_dp(x), _dp(y), B, N, H, d, dt, dh, dw, Hl, Wl, start_frame,
-                              theta, round_mode, nthreads or default_threads())
+                              theta, round_mode, int(bool(f32_eval)), nthreads or default_threads())
     return y
 
 
@@ -207,7 +222,8 @@ class ReuseBook:
 class OracleRun:
     """Runs the method step by step for a chosen list of query rows (b, h, r).
 
-    Each step: optional RoPE on q and k (rounded to the attention input dtype), fresh states
+    Each step: optional RoPE on q and k (evaluated in fp32 and rounded to the attention input
+    dtype when that dtype is bf16/fp32; in fp64 when input_round is ROUND_NONE), fresh states
     for the computed pairs written into the per-row cache (O rounded to the cache dtype, lse
     kept in fp32), then the merge of all P cached states of each row.
     """
@@ -232,7 +248,8 @@ class OracleRun:
     def rotate(self, x: np.ndarray) -> np.ndarray:
         r = self.rope
         return rope_apply(x, r["Hl"], r["Wl"], r.get("start_frame", 0), r["dt"], r["dh"],
-                          r["dw"], r.get("theta", 10000.0), self.input_round, self.nthreads)
+                          r["dw"], r.get("theta", 10000.0), self.input_round,
+                          self.input_round != ROUND_NONE, self.nthreads)
 
     def step(self, q: np.ndarray, k: np.ndarray, v: np.ndarray, reuse=None):
         """q, k, v: float arrays [B, N, H, d] holding the config-dtype values."""

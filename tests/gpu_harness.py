@@ -8,12 +8,18 @@ oracle's rows:
   * that cache slots of reused pairs are bit-identical to before the step (reuse moves nothing);
   * the plan's bookkeeping (valid, step computed, steps run) against the oracle's, bit-exact.
 
-Tolerances (max absolute error): fp32 workloads 1e-4 for outputs and lse; bf16 workloads 2e-2
-for outputs and states (both sides' values expressed in bf16: the oracle's fp64 output is
-rounded to bf16 before the comparison, as the library stores its output in bf16) and 1e-3 for
-lse.
+Tolerances: fp32 workloads 1e-4 max-abs for outputs, states and lse; bf16 workloads 2e-2
+max-abs for outputs and 1e-3 for lse. The cached per-pair states are internal bf16 values with
+no stated tolerance; they are held to 2e-2 relative to max(1, |value|), i.e. the output
+tolerance below magnitude 1 and bf16's relative resolution above it. The library's bf16 values are compared
+with the oracle's unrounded fp64 values, so the library's own final rounding (at most half a
+bf16 ulp) is part of the error; rounding the oracle as well would double the rounding error.
+The oracle's merge itself reads its cache rounded to the cache dtype, as the library does.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -125,14 +131,11 @@ class ParityRun:
         out = self.out[self.b_idx, self.r_idx, self.h_idx].float().cpu().numpy()
         lse = self.out_lse[self.b_idx, self.h_idx, self.r_idx].cpu().numpy()
         ref_out = res["out"]
-        if w.dtype == "bf16":
-            ref_out = oracle.round_bf16(ref_out)
         err = {"out": float(np.abs(out - ref_out).max()),
                "lse": float(np.abs(lse - res["out_lse"]).max())}
         O_after, L_after = self.gather_cache()
         comp = mask[self.part] == 0            # [rows, P] computed pairs of each row
-        ref_O = self.orc.cache_O               # rounded to the cache dtype
-        e_state = np.abs(O_after - ref_O)[comp]
+        e_state = (np.abs(O_after - res["fresh_O"]) / np.maximum(1.0, np.abs(res["fresh_O"])))[comp]
         e_lse = np.abs(L_after - res["fresh_lse"])[comp]
         err["state_O"] = float(e_state.max()) if e_state.size else 0.0
         err["state_lse"] = float(e_lse.max()) if e_lse.size else 0.0
@@ -147,4 +150,10 @@ class ParityRun:
               err["state_O"] <= tol["out"] and err["state_lse"] <= tol["lse"] and
               err["reused_changed"] == 0 and err["book_equal"])
         err["ok"] = ok
+        err["step"] = self.t - 1
+        err["workload"] = w.name
+        log = os.environ.get("DITANGO_PARITY_LOG")
+        if log:
+            with open(log, "a") as f:
+                f.write(json.dumps(err) + "\n")
         return err
