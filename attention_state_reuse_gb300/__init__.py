@@ -32,7 +32,8 @@ SYMBOLS = [
     "ditango_plan", "ditango_plan_destroy", "ditango_plan_set_mask", "ditango_plan_check_mask",
     "ditango_plan_get_offsets", "ditango_plan_get_pairs", "ditango_plan_get_cache_state",
     "ditango_plan_set_profile_events",
-    "ditango_attn_step", "ditango_attn_step_workspace_size", "ditango_merge",
+    "ditango_attn_step", "ditango_attn_step_static_workspace",
+    "ditango_attn_step_workspace_size", "ditango_merge",
     "ditango_rope_build_tables", "ditango_device_status", "ditango_status_string",
     "ditango_version",
 ]
@@ -94,6 +95,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ditango_attn_step.argtypes = [vp, P(Tensor), P(Tensor), P(Tensor), P(Rope), u8p,
                                       P(StateCache), P(Tensor), P(Tensor), ctypes.c_float, vp,
                                       ctypes.c_size_t, vp]
+    lib.ditango_attn_step_static_workspace.argtypes = [vp, P(Tensor), P(Tensor), P(Tensor),
+                                                       P(Rope), u8p, P(StateCache), P(Tensor),
+                                                       P(Tensor), ctypes.c_float, vp]
     lib.ditango_attn_step_workspace_size.argtypes = [vp, i64, i64, i32, i32, i32]
     lib.ditango_attn_step_workspace_size.restype = ctypes.c_size_t
     lib.ditango_merge.argtypes = [P(StateList), P(Tensor), P(Tensor), vp]
@@ -302,6 +306,27 @@ def attn_step(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None, reuse_
         ctypes.byref(ld) if ld is not None else None, ctypes.c_float(softmax_scale), ws_ptr,
         ws_bytes, _stream_ptr(stream))
     _check(st, "ditango_attn_step")
+
+
+def attn_step_static_workspace(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None,
+                               reuse_mask=None, rope: RopeTables | None = None,
+                               softmax_scale: float | None = None, stream=None) -> None:
+    """ditango_attn_step_static_workspace: the step without a caller workspace, for callers
+    that cannot allocate device memory; its scratch lives in a 64 MiB array inside the
+    library (steps needing more are refused with WORKSPACE). Concurrent calls race on it."""
+    if softmax_scale is None:
+        softmax_scale = q.shape[-1] ** -0.5
+    qd, kd, vd, od = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
+    cache = StateCache(tensor_desc(cache_O), tensor_desc(cache_lse))
+    ld = tensor_desc(out_lse) if out_lse is not None else None
+    rs = rope.struct() if rope is not None else None
+    arr, mptr = _mask_ptr(reuse_mask, plan.P)
+    st = _lib().ditango_attn_step_static_workspace(
+        plan.handle, ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd),
+        ctypes.byref(rs) if rs is not None else None, mptr, ctypes.byref(cache), ctypes.byref(od),
+        ctypes.byref(ld) if ld is not None else None, ctypes.c_float(softmax_scale),
+        _stream_ptr(stream))
+    _check(st, "ditango_attn_step_static_workspace")
 
 
 def merge(O_states, lse_states, out, out_lse=None, stream=None) -> None:

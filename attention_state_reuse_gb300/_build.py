@@ -14,7 +14,8 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libditango.so")
 OBJ_DIR = os.path.join(PKG, "_lib", "obj")
 
-SOURCES = ["api.cu", "plan.cpp", "pair_tc.cu", "pair_f32.cu", "merge.cu", "rope.cu"]
+SOURCES = ["api.cu", "plan.cpp", "pair_tc.cu", "pair_f32.cu", "merge.cu", "rope.cu",
+           "attn_step_static.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

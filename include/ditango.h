@@ -178,6 +178,28 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
                       float softmax_scale, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/* The same step for callers that cannot allocate device memory (the paper has no counterpart
+ * to this entry point; it exists for the library's users). Some callers cannot call cudaMalloc:
+ * plugins whose host framework forbids device allocation during execution, processes whose
+ * memory pool already holds the GPU's free memory, latency-critical loops that cannot take
+ * cudaMalloc's implicit synchronisation. Arguments and errors are those of ditango_attn_step,
+ * without the workspace: the step's scratch (the rotated q and k when rope != NULL) lives in
+ * a 64 MiB device array inside the library, held on every GPU where the library's device code
+ * is loaded until the process exits. Steps whose scratch exceeds 64 MiB
+ * (ditango_attn_step_workspace_size > 64 MiB, i.e. more than 2^24 bf16 elements per rotated
+ * tensor) return DITANGO_ERR_WORKSPACE before launching anything. Allocates nothing (no
+ * cudaMalloc/cudaFree). The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress), so make it before any stream capture on that device. Every call
+ * shares the one array and it keeps the last call's contents; nothing in it needs to start
+ * at zero (each call writes every byte it reads), but calls whose work overlaps on the GPU
+ * (other streams, other threads) race on it. */
+int ditango_attn_step_static_workspace(ditango_plan_t plan, const ditango_tensor* q,
+                                       const ditango_tensor* k, const ditango_tensor* v,
+                                       const ditango_rope* rope, const uint8_t* reuse_mask,
+                                       const ditango_state_cache* cache, const ditango_tensor* out,
+                                       const ditango_tensor* out_lse, float softmax_scale,
+                                       void* stream);
+
 /* Bytes of workspace ditango_attn_step needs for these shapes (0 without RoPE). */
 size_t ditango_attn_step_workspace_size(ditango_plan_t plan, int64_t B, int64_t H, int32_t d,
                                         int32_t dtype, int32_t use_rope);
