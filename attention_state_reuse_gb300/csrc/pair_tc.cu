@@ -109,10 +109,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // Issues O_w (+)= P_w V for the tile before the current one: waits for P_w of that tile, for
 // the epilogue of the previous partition to have read O_w (first tile of a partition), and
 // for the V tile; then eight K=16 steps with A read from TMEM (P) and B = V (MN-major).
+// v_lo0 is the low descriptor half of ring slot 0 for an MN-major operand.
 template <int D>
 __device__ __forceinline__ bool issue_pv(SharedCtl<Cfg<D>::STAGES>* ctl, int w, uint32_t prev_g,
                                          uint32_t prev_v, uint32_t prev_pidx, bool prev_first,
-                                         uint32_t kv_addr, uint32_t tbase, volatile int* abort_w) {
+                                         uint32_t v_lo0, uint32_t desc_hi, uint32_t tbase,
+                                         volatile int* abort_w) {
   using C = Cfg<D>;
   constexpr int STAGES = C::STAGES;
   if (!mbar_wait(&ctl->p_full[w], prev_g & 1u, abort_w)) return false;
@@ -121,15 +123,33 @@ __device__ __forceinline__ bool issue_pv(SharedCtl<Cfg<D>::STAGES>* ctl, int w, 
   if (w == 0 && !mbar_wait(&ctl->kv_full[prev_v % STAGES], (prev_v / STAGES) & 1u, abort_w))
     return false;
   tc_fence_after_sync();
-  const uint32_t v_addr = kv_addr + (prev_v % STAGES) * C::TILE_BYTES;
+  const uint32_t v_lo = v_lo0 + (prev_v % STAGES) * (C::TILE_BYTES >> 4);
+  const uint32_t d_t = tbase + C::o_col(w);
+  const uint32_t a_t = tbase + C::s_col(w);
+  if (prev_first)
+    mma_ts<0>(d_t, a_t, v_lo, desc_hi, C::IDESC_PV);
+  else
+    mma_ts<1>(d_t, a_t, v_lo, desc_hi, C::IDESC_PV);
 #pragma unroll
-  for (int k = 0; k < kTileRows / 16; ++k) {
-    const uint64_t bdesc = sdesc_sw128(v_addr + k * 2048, kChunkBytes, 1024);
-    mma_bf16_ts(tbase + C::o_col(w), tbase + C::s_col(w) + k * 8, bdesc, C::IDESC_PV,
-                (k > 0 || !prev_first) ? 1u : 0u);
-  }
+  for (int k = 1; k < kTileRows / 16; ++k)  // 16 KV rows (2048 bytes) per step
+    mma_ts<1>(d_t, a_t + k * 8, v_lo + k * (2048 >> 4), desc_hi, C::IDESC_PV);
   tc_commit(&ctl->o_done[w]);
   return true;
+}
+
+// Low descriptor-half offset of K step k (16 elements) inside a K-major 128-byte-swizzled
+// operand whose K extent is split into 64-element chunks kChunkBytes apart.
+__host__ __device__ constexpr uint32_t kstep_off(int k) {
+  return static_cast<uint32_t>(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4);
+}
+
+// S_w = Q_w K^T for the K tile at low descriptor half k_lo: D/16 steps, both operands K-major.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_t, uint32_t q_lo, uint32_t k_lo, uint32_t hi) {
+  mma_ss<0>(d_t, q_lo, hi, k_lo, hi, Cfg<D>::IDESC_QK);
+#pragma unroll
+  for (int k = 1; k < D / 16; ++k)
+    mma_ss<1>(d_t, q_lo + kstep_off(k), hi, k_lo + kstep_off(k), hi, Cfg<D>::IDESC_QK);
 }
 
 template <int D>
@@ -229,8 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t e = 0, uc = 0, g = 0, pidx = 0;
       bool ok = true;
-      const uint32_t q_addr = smem_u32(q_smem);
-      const uint32_t kv_addr = smem_u32(kv_smem);
+      const uint32_t desc_hi = sdesc_sw128_hi(1024);  // SBO: 8 rows of 128 bytes
+      const uint32_t q_lo0 = sdesc_sw128_lo(smem_u32(q_smem), 16);
+      const uint32_t q_lo1 = q_lo0 + (C::TILE_BYTES >> 4);
+      const uint32_t k_lo0 = sdesc_sw128_lo(smem_u32(kv_smem), 16);
+      const uint32_t v_lo0 = sdesc_sw128_lo(smem_u32(kv_smem), kChunkBytes);  // LBO: next 64 ch
       for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x, ++uc) {
         const UnitInfo ui = decode_unit(sch, u);
         ok = mbar_wait(&ctl->q_full, uc & 1u, abort_w);
@@ -247,16 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&ctl->kv_full[ke % STAGES], (ke / STAGES) & 1u, abort_w);
             if (!ok) break;
             tc_fence_after_sync();
-            const uint32_t k_addr = kv_addr + (ke % STAGES) * C::TILE_BYTES;
+            const uint32_t k_lo = k_lo0 + (ke % STAGES) * (C::TILE_BYTES >> 4);
             for (int w = 0; w < 2; ++w) {
-              if (have_prev && !(ok = issue_pv<D>(ctl, w, prev_g, prev_v, prev_pidx, prev_first, kv_addr, tbase, abort_w))) break;
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-                const uint64_t adesc = sdesc_sw128(q_addr + w * C::TILE_BYTES + off, 16, 1024);
-                const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
-                mma_bf16_ss(tbase + C::s_col(w), adesc, bdesc, C::IDESC_QK, k > 0 ? 1u : 0u);
-              }
+              if (have_prev && !(ok = issue_pv<D>(ctl, w, prev_g, prev_v, prev_pidx, prev_first,
+                                                  v_lo0, desc_hi, tbase, abort_w)))
+                break;
+              issue_qk<D>(tbase + C::s_col(w), w ? q_lo1 : q_lo0, k_lo, desc_hi);
               tc_commit(&ctl->s_full[w]);
             }
             if (!ok) break;
@@ -274,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&ctl->q_empty);  // every Q K^T of this unit has been issued
         if (!have_prev) continue;  // a unit always visits its own partition; kept for safety
         for (int w = 0; ok && w < 2; ++w)
-          ok = issue_pv<D>(ctl, w, prev_g, prev_v, prev_pidx, prev_first, kv_addr, tbase, abort_w);
+          ok = issue_pv<D>(ctl, w, prev_g, prev_v, prev_pidx, prev_first, v_lo0, desc_hi, tbase,
+                           abort_w);
         if (!ok) break;
         tc_commit(&ctl->kv_empty[prev_v % STAGES]);
       }
@@ -318,9 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kTileRows; ++c)
               if (c >= valid) s[c] = -INFINITY;
           }
-          float mx = s[0];
+          // row max: eight independent three-input max chains, then a short tree
+          float m8[8];
 #pragma unroll
-          for (int c = 1; c < kTileRows; ++c) mx = fmaxf(mx, s[c]);
+          for (int x = 0; x < 8; ++x) m8[x] = fmaxf(s[x], s[8 + x]);
+#pragma unroll
+          for (int c = 16; c < kTileRows; c += 16)
+#pragma unroll
+            for (int x = 0; x < 8; ++x) m8[x] = fmax3(m8[x], s[c + x], s[c + 8 + x]);
+          const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                 fmaxf(m8[6], m8[7]));
           const float m_tile = mx * sl2;
           bool need_rescale = false;
           float alpha = 1.f;
@@ -347,22 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st_32x32b_x32(o_taddr + c * 32, r);
             }
           }
-          const float neg_m = -m_run;
-          float lsum0 = 0.f, lsum1 = 0.f;
+          // p = 2^(s * scale * log2(e) - m): paired fp32 FMA/add instructions halve the ALU
+          // issue of the scale-subtract and of the row sum (four independent pair sums); the
+          // exponentials go to the SFU, which competes far less with tensor-core issue
+          const float2 sl2x2 = make_float2(sl2, sl2);
+          const float2 negm2 = make_float2(-m_run, -m_run);
+          float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const float p0 = ex2_approx(fmaf(s[64 * half + 2 * c], sl2, neg_m));
-              const float p1 = ex2_approx(fmaf(s[64 * half + 2 * c + 1], sl2, neg_m));
-              lsum0 += p0;
-              lsum1 += p1;
+              const int e0 = 64 * half + 2 * c;
+              const float2 x = __ffma2_rn(make_float2(s[e0], s[e0 + 1]), sl2x2, negm2);
+              const float p0 = ex2_approx(x.x);
+              const float p1 = ex2_approx(x.y);
+              l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
               pk[c] = pack_bf16x2(p0, p1);
             }
             tmem_st_32x32b_x32(s_taddr + 32 * half, pk);
           }
-          l_run += lsum0 + lsum1;
+          const float2 l2 = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+          l_run += l2.x + l2.y;
           tmem_st_wait();
           tc_fence_before_sync();
           mbar_arrive(&ctl->p_full[w]);

@@ -12,8 +12,8 @@
 // angle = pos * theta^(-2k/d_a): (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos).
 // Token n sits at t = n / (Hl Wl) + s, h = (n / Wl) mod Hl, w = n mod Wl.
 //
-// rope_apply_kernel: memory bound; one thread rotates 8 channels (4 pairs) of one (b, n, h),
-// reading 16 bytes and writing 16 bytes (bf16). The rotation is evaluated in fp32 as
+// rope_apply_kernel: memory bound; a thread rotates the 16-byte vector (8 bf16 or 4 fp32
+// channels) of one (token, head), reading and writing 16 bytes. The rotation is evaluated in fp32 as
 // y0 = fl(fl(x0 c) - fl(x1 s)), y1 = fl(fl(x0 s) + fl(x1 c)) with fp32 tables c, s, then
 // rounded (nearest-even) to the storage dtype.
 #include <cuda_bf16.h>
@@ -24,83 +24,88 @@ namespace ditango {
 namespace {
 
 constexpr int kRopeThreads = 256;
-constexpr int kPairsPerThread = 4;
+constexpr int kMaxPairs = 64;  // d <= 128
 
-
-__device__ __forceinline__ void pair_table(const RopeApplyArgs& a, int m, int64_t t, int64_t h,
-                                           int64_t w, float& cs, float& sn) {
-  const int ht = a.dt / 2, hh = a.dh / 2, hw = a.dw / 2;
-  if (m < ht) {
-    cs = __ldg(a.cos_t + t * ht + m);
-    sn = __ldg(a.sin_t + t * ht + m);
-  } else if (m < ht + hh) {
-    cs = __ldg(a.cos_h + h * hh + (m - ht));
-    sn = __ldg(a.sin_h + h * hh + (m - ht));
-  } else {
-    cs = __ldg(a.cos_w + w * hw + (m - ht - hh));
-    sn = __ldg(a.sin_w + w * hw + (m - ht - hh));
-  }
-}
-
+// One block per token at a time (grid-stride over tokens): the token's position (t, h, w) is
+// decoded once, the cos/sin of its d/2 channel pairs are staged in shared memory, then the
+// block streams every head of q and k for that token with 16-byte vectors (the rows of one
+// token are contiguous across heads, so the loads and stores are fully coalesced).
 template <typename T>
 __global__ void __launch_bounds__(kRopeThreads) rope_apply_kernel(const __grid_constant__ RopeApplyArgs a) {
-  const int groups = a.d / (2 * kPairsPerThread);  // threads per (b, n, h)
-  const int64_t per_tensor = a.B * a.N * a.H * groups;
-  const int64_t total = per_tensor * a.n_tensors;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int which = static_cast<int>(idx / per_tensor);
-    int64_t rem = idx - which * per_tensor;
-    const int grp = static_cast<int>(rem % groups);
-    rem /= groups;
-    const int64_t hd = rem % a.H;
-    rem /= a.H;
-    const int64_t n = rem % a.N;
-    const int64_t b = rem / a.N;
-    const int64_t hw_tokens = a.Hl * a.Wl;
-    const int64_t t = n / hw_tokens + a.start_frame;
-    const int64_t hh = (n / a.Wl) % a.Hl;
-    const int64_t ww = n % a.Wl;
-    const T* src = static_cast<const T*>(a.x[which]) + b * a.xs[which][0] + n * a.xs[which][1] +
-                   hd * a.xs[which][2] + grp * 2 * kPairsPerThread;
-    T* dst = static_cast<T*>(a.y[which]) + ((b * a.N + n) * a.H + hd) * a.d + grp * 2 * kPairsPerThread;
-    float x[2 * kPairsPerThread];
-    if constexpr (sizeof(T) == 2) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(wv[i] << 16);
-        x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+  constexpr int VEC = 16 / sizeof(T);  // channels per 16-byte vector
+  __shared__ float cs_s[kMaxPairs], sn_s[kMaxPairs];
+  const int pairs = a.d / 2;
+  const int ht = a.dt / 2, hh = a.dh / 2, hw = a.dw / 2;
+  const int vpr = a.d / VEC;  // vectors per (token, head)
+  const int per_tensor = static_cast<int>(a.H) * vpr;
+  const int per_token = a.n_tensors * per_tensor;
+  const int64_t tokens = a.B * a.N;
+  const int hw_tokens = static_cast<int>(a.Hl * a.Wl);
+  for (int64_t tok = blockIdx.x; tok < tokens; tok += gridDim.x) {
+    const int64_t b = tok / a.N;
+    const int n = static_cast<int>(tok - b * a.N);
+    const int t = n / hw_tokens + static_cast<int>(a.start_frame);
+    const int hp = (n / static_cast<int>(a.Wl)) % static_cast<int>(a.Hl);
+    const int wp = n % static_cast<int>(a.Wl);
+    __syncthreads();  // the previous token's tables are no longer read
+    for (int m = threadIdx.x; m < pairs; m += blockDim.x) {
+      float c, sn;
+      if (m < ht) {
+        c = __ldg(a.cos_t + t * ht + m);
+        sn = __ldg(a.sin_t + t * ht + m);
+      } else if (m < ht + hh) {
+        c = __ldg(a.cos_h + hp * hh + (m - ht));
+        sn = __ldg(a.sin_h + hp * hh + (m - ht));
+      } else {
+        c = __ldg(a.cos_w + wp * hw + (m - ht - hh));
+        sn = __ldg(a.sin_w + wp * hw + (m - ht - hh));
       }
-    } else {
-      const float4 v0 = __ldg(reinterpret_cast<const float4*>(src));
-      const float4 v1 = __ldg(reinterpret_cast<const float4*>(src) + 1);
-      x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-      x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+      cs_s[m] = c;
+      sn_s[m] = sn;
     }
-    float y[2 * kPairsPerThread];
+    __syncthreads();
+    for (int v = threadIdx.x; v < per_token; v += blockDim.x) {
+      const int which = v >= per_tensor ? 1 : 0;
+      const int rem = v - which * per_tensor;
+      const int hd = rem / vpr;
+      const int grp = rem - hd * vpr;
+      const T* __restrict__ src = static_cast<const T*>(a.x[which]) + b * a.xs[which][0] +
+                                  static_cast<int64_t>(n) * a.xs[which][1] + hd * a.xs[which][2] +
+                                  grp * VEC;
+      T* __restrict__ dst = static_cast<T*>(a.y[which]) + (tok * a.H + hd) * a.d + grp * VEC;
+      float x[VEC];
+      if constexpr (sizeof(T) == 2) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int p = 0; p < kPairsPerThread; ++p) {
-      const int m = grp * kPairsPerThread + p;
-      float cs, sn;
-      pair_table(a, m, t, hh, ww, cs, sn);
-      // explicit round-to-nearest products and sums (never contracted into FMA), so that the
-      // rotated value rounded to the storage dtype is a reproducible fp32 result
-      y[2 * p] = __fsub_rn(__fmul_rn(x[2 * p], cs), __fmul_rn(x[2 * p + 1], sn));
-      y[2 * p + 1] = __fadd_rn(__fmul_rn(x[2 * p], sn), __fmul_rn(x[2 * p + 1], cs));
-    }
-    if constexpr (sizeof(T) == 2) {
-      uint32_t wv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
-        wv[i] = *reinterpret_cast<uint32_t*>(&h2);
+        for (int i = 0; i < 4; ++i) {
+          x[2 * i] = __uint_as_float(wv[i] << 16);
+          x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        }
+      } else {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(src));
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
       }
-      *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    } else {
-      reinterpret_cast<float4*>(dst)[0] = make_float4(y[0], y[1], y[2], y[3]);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(y[4], y[5], y[6], y[7]);
+      float y[VEC];
+#pragma unroll
+      for (int p = 0; p < VEC / 2; ++p) {
+        const float c = cs_s[grp * (VEC / 2) + p], sn = sn_s[grp * (VEC / 2) + p];
+        // explicit round-to-nearest products and sums (never contracted into FMA), so that the
+        // rotated value rounded to the storage dtype is a reproducible fp32 result
+        y[2 * p] = __fsub_rn(__fmul_rn(x[2 * p], c), __fmul_rn(x[2 * p + 1], sn));
+        y[2 * p + 1] = __fadd_rn(__fmul_rn(x[2 * p], sn), __fmul_rn(x[2 * p + 1], c));
+      }
+      if constexpr (sizeof(T) == 2) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+          wv[i] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      } else {
+        *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+      }
     }
   }
 }
@@ -125,10 +130,11 @@ __global__ void rope_tables_kernel(float* c, float* s, int64_t rows, int32_t hal
 }  // namespace
 
 cudaError_t launch_rope_apply(const RopeApplyArgs& a, cudaStream_t stream) {
-  const int64_t total = a.B * a.N * a.H * (a.d / (2 * kPairsPerThread)) * a.n_tensors;
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
-  if (blocks > 152 * 32) blocks = 152 * 32;  // grid-stride beyond 32 waves of the SM count
+  const int64_t tokens = a.B * a.N;
+  if (tokens == 0 || a.n_tensors == 0) return cudaSuccess;
+  if (a.d / 2 > kMaxPairs) return cudaErrorInvalidValue;
+  // up to 16 blocks of 256 threads per SM (152 SMs); each block walks many tokens
+  const int64_t blocks = tokens < 152 * 16 ? tokens : 152 * 16;
   if (a.dtype == DITANGO_BF16)
     rope_apply_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kRopeThreads, 0, stream>>>(a);
   else

@@ -431,11 +431,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of host CPU work for the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count (smaller cases for profiler captures)")
     args = ap.parse_args()
 
     from attention_state_reuse_gb300 import workloads as wl
 
     w = wl.get(args.workload)
+    if args.heads is not None and args.heads != w.H:
+        w = wl.scaled(w, f"{w.name}_h{args.heads}", H=args.heads)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
 
