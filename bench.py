@@ -259,6 +259,8 @@ def run_ours(args, w, rank, world):
     h2d = 3 * B * N * H * d * esz
     d2h = B * N * H * d * esz + B * H * N * 4
 
+    sweep = reuse_sweep(dev) if (args.sweep and world == 1) else None
+
     flops = pair_flops(w, mask)
     peaks, peak_src = load_peaks()
     tc_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
@@ -296,9 +298,83 @@ def run_ours(args, w, rank, world):
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * (3 if w.rope else 2),
+        "reuse_sweep": sweep,
         "clocks": ck,
     }
     return line
+
+
+def reuse_sweep(dev, steps=10):
+    """Step time against the fraction of reused pairs (the reuse-fraction sweep workload).
+
+    N = 32760 (21x30x52 latent), H = 40, d = 128, bf16, P in {4, 8, 16}, no RoPE, seeded
+    N(0,1) inputs. Masks: every distance threshold |i - j| >= D from D = P (all pairs
+    computed) down to the smallest D with at most 87.5% of pairs reused, plus the seeded random
+    mask (reuse probability 0.5, local pairs always computed). After an all-compute anchor
+    step, each mask is timed over `steps` steps (CUDA events, inputs larger than L2). Reports
+    ms/step, effective TFLOP/s over computed pairs, the pair kernel's time, and per P a
+    least-squares fit ms = a * computed_fraction + b with its R^2.
+    """
+    import numpy as np
+    import torch
+
+    import attention_state_reuse_gb300 as dt
+    from attention_state_reuse_gb300 import workloads as wl
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record()
+    w0 = wl.get("sweep_P8")
+    q, k, v = (torch.from_numpy(a).to(dev).to(torch.bfloat16) for a in wl.InputStream(w0).next())
+    out = torch.empty_like(q)
+    out_lse = torch.empty((w0.B, w0.H, w0.N), dtype=torch.float32, device=dev)
+    result = {}
+    for P in (4, 8, 16):
+        w = wl.get(f"sweep_P{P}")
+        plan = dt.Plan(w.N, P)
+        cO, cL = dt.new_state_cache(w.B, w.H, P, w.N, w.d, torch.bfloat16, dev)
+        step = lambda m: dt.attn_step(plan, q, k, v, cO, cL, out, out_lse, reuse_mask=m,
+                                      softmax_scale=w.scale)
+        masks = []
+        for kind in w.schedule:
+            if kind[0] == "all":
+                masks.append(("all computed", wl.distance_mask(P, P)))
+            elif kind[0] == "dist":
+                masks.append((f"|i-j|>={kind[1]}", wl.distance_mask(P, kind[1])))
+            else:
+                masks.append(("random p=0.5", wl.random_mask(P, 1000 * w.index + 7 + P)))
+        step(masks[0][1])  # anchor
+        rows = []
+        for name, m in masks:
+            step(m)
+            torch.cuda.synchronize()
+            plan.set_profile_events(evs)
+            t0.record()
+            for _ in range(steps):
+                step(m)
+            t1.record()
+            torch.cuda.synchronize()
+            pair_ms = evs[1].elapsed_time(evs[2])  # last step's pair kernel
+            plan.set_profile_events(None)
+            ms = t0.elapsed_time(t1) / steps
+            f = pair_flops(w, m)
+            rows.append({"mask": name, "reuse_fraction": round(float(np.asarray(m).mean()), 4),
+                         "ms": round(ms, 4), "effective_tflops": round(f / (ms * 1e-3) / 1e12, 1),
+                         "pair_ms": round(pair_ms, 4),
+                         "pair_tflops": round(f / (pair_ms * 1e-3) / 1e12, 1)})
+        dist = [r for r in rows if r["mask"] != "random p=0.5"]
+        comp = np.array([1.0 - r["reuse_fraction"] for r in dist])
+        msv = np.array([r["ms"] for r in dist])
+        a, b = np.polyfit(comp, msv, 1)
+        pred = a * comp + b
+        r2 = 1.0 - ((msv - pred) ** 2).sum() / max(((msv - msv.mean()) ** 2).sum(), 1e-12)
+        result[f"P{P}"] = {"points": rows,
+                           "fit": {"ms_per_computed_fraction": round(float(a), 4),
+                                   "ms_at_full_reuse": round(float(b), 4), "r2": round(float(r2), 5)}}
+        del cO, cL, plan
+        torch.cuda.empty_cache()
+    return result
 
 
 def barrier(world):
@@ -431,6 +507,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of host CPU work for the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="skip the reuse-fraction sweep")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (smaller cases for profiler captures)")
     args = ap.parse_args()
