@@ -2,7 +2,8 @@
 //
 // One attention-layer step (DiTango, gist.science/paper/2607.15650, Methodology 1-2):
 //   1. validate the reuse mask against the plan's cache bookkeeping (host);
-//   2. optional 3D RoPE of q and k into the caller's workspace (rope.cu);
+//   2. optional 3D RoPE: k (and q for fp32) into the caller's workspace (rope.cu); for bf16
+//      the pair kernel rotates each Q tile in shared memory after loading it (pair_tc.cu);
 //   3. fresh states for the computed pairs only, written into the state cache (pair_tc.cu for
 //      bf16, pair_f32.cu for fp32), over a schedule that lists computed pairs only;
 //   4. merge of all P cached states of every query row (merge.cu);
@@ -118,10 +119,17 @@ int check_rope(const ditango_rope* r, int64_t N, int64_t d) {
   return DITANGO_OK;
 }
 
-size_t rope_workspace_bytes(int64_t B, int64_t N, int64_t H, int64_t d, int32_t dtype) {
+// Bytes of one rotated [B, N, H, d] copy, rounded up to 256.
+size_t rope_copy_bytes(int64_t B, int64_t N, int64_t H, int64_t d, int32_t dtype) {
   const size_t one = static_cast<size_t>(B * N * H * d) * elem_size(dtype);
-  const size_t one_aligned = (one + 255) & ~static_cast<size_t>(255);
-  return 2 * one_aligned;
+  return (one + 255) & ~static_cast<size_t>(255);
+}
+
+// Room for the rotated k and the rotated q. The BF16 pair kernel rotates q itself whenever the
+// table rows fit its shared memory and then leaves the second half unused; the size does not
+// depend on that, so that a caller's buffer stays valid for any table shape.
+size_t rope_workspace_bytes(int64_t B, int64_t N, int64_t H, int64_t d, int32_t dtype) {
+  return 2 * rope_copy_bytes(B, N, H, d, dtype);
 }
 
 }  // namespace
@@ -196,21 +204,40 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   };
   if (!mark(0)) return DITANGO_ERR_CUDA;
 
-  // ---- 1. rotary prologue into the workspace
+  // ---- 1. rotary prologue into the workspace: k (and, for F32, q); the BF16 pair kernel
+  // rotates each Q tile itself after loading it
   const void* qp = q->ptr;
   const void* kp = k->ptr;
   int64_t qs[4] = {q->stride[0], q->stride[1], q->stride[2], 1};
   int64_t ks[4] = {k->stride[0], k->stride[1], k->stride[2], 1};
+  // the BF16 pair kernel rotates Q itself when the table rows fit its shared memory
+  RopeQ rq;
+  std::memset(&rq, 0, sizeof(rq));
+  if (rope != nullptr && dtype == DITANGO_BF16) {
+    auto odd = [](int32_t x) { return x | 1; };
+    rq.cos_t = rope->cos_t; rq.sin_t = rope->sin_t;
+    rq.cos_h = rope->cos_h; rq.sin_h = rope->sin_h;
+    rq.cos_w = rope->cos_w; rq.sin_w = rope->sin_w;
+    rq.Hl = static_cast<int32_t>(rope->Hl);
+    rq.Wl = static_cast<int32_t>(rope->Wl);
+    rq.start_frame = static_cast<int32_t>(rope->start_frame);
+    rq.dt = rope->dt; rq.dh = rope->dh; rq.dw = rope->dw;
+    rq.nT = static_cast<int32_t>(N / (rope->Hl * rope->Wl));
+    rq.sT = odd(rope->dt / 2); rq.sH = odd(rope->dh / 2); rq.sW = odd(rope->dw / 2);
+    const int64_t pairs = int64_t{rq.nT} * rq.sT + rope->Hl * rq.sH + rope->Wl * rq.sW;
+    rq.n_pairs = 8 * pairs <= kRopeSmemMaxBytes ? static_cast<int32_t>(pairs) : 0;
+  }
+  const bool q_in_kernel = rq.n_pairs > 0;
   if (rope != nullptr) {
-    const size_t one = rope_workspace_bytes(B, N, H, d, dtype) / 2;
+    const size_t one = rope_copy_bytes(B, N, H, d, dtype);
     RopeApplyArgs ra;
     std::memset(&ra, 0, sizeof(ra));
-    ra.n_tensors = 2;
-    ra.x[0] = q->ptr;
-    ra.x[1] = k->ptr;
+    ra.n_tensors = q_in_kernel ? 1 : 2;
+    ra.x[0] = k->ptr;
+    ra.x[1] = q->ptr;
     for (int a = 0; a < 3; ++a) {
-      ra.xs[0][a] = q->stride[a];
-      ra.xs[1][a] = k->stride[a];
+      ra.xs[0][a] = k->stride[a];
+      ra.xs[1][a] = q->stride[a];
     }
     ra.y[0] = workspace;
     ra.y[1] = static_cast<uint8_t*>(workspace) + one;
@@ -222,11 +249,13 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     ra.Hl = rope->Hl; ra.Wl = rope->Wl; ra.start_frame = rope->start_frame;
     ra.dt = rope->dt; ra.dh = rope->dh; ra.dw = rope->dw;
     if (launch_rope_apply(ra, s) != cudaSuccess) return DITANGO_ERR_CUDA;
-    qp = ra.y[0];
-    kp = ra.y[1];
     const int64_t cs[4] = {N * H * d, H * d, d, 1};
-    std::memcpy(qs, cs, sizeof(cs));
+    kp = ra.y[0];
     std::memcpy(ks, cs, sizeof(cs));
+    if (!q_in_kernel) {
+      qp = ra.y[1];
+      std::memcpy(qs, cs, sizeof(cs));
+    }
   }
 
   // ---- 2. fresh states of the computed pairs
@@ -249,6 +278,7 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     pa.cache_lse = static_cast<float*>(cL.ptr);
     pa.scale_log2 = softmax_scale * 1.4426950408889634f;
     pa.err = dev->err_ptr;
+    pa.rope = rq;
     if (launch_pair_tc(static_cast<int>(d), mq, mk, mv, pa, dev->num_sms, s) != cudaSuccess)
       return DITANGO_ERR_CUDA;
   } else {

@@ -34,6 +34,20 @@ struct PairSchedule {
 void build_schedule(int64_t N, int32_t P, const int64_t* offsets, const uint8_t* mask, int64_t B,
                     int64_t H, int32_t block_rows, PairSchedule* s);
 
+// 3D RoPE tables for rotating Q inside the pair kernel (see rope.cu for the definition). The
+// kernel copies the rows it can need into shared memory as (cos, sin) pairs: nT frame rows
+// (frames start_frame .. start_frame + nT - 1) of stride sT, then Hl rows of stride sH, then
+// Wl rows of stride sW (strides in pairs, odd so that a warp's 32 rows hit distinct banks).
+struct RopeQ {
+  const float *cos_t, *sin_t, *cos_h, *sin_h, *cos_w, *sin_w;
+  int32_t Hl, Wl, start_frame;
+  int32_t dt, dh, dw;
+  int32_t nT, sT, sH, sW;
+  int32_t n_pairs;  // nT*sT + Hl*sH + Wl*sW; 0: q is used as given
+};
+// Shared memory the pair kernel may give the tables; larger tables keep Q in the pre-pass.
+constexpr int kRopeSmemMaxBytes = 32768;
+
 // bf16 pair kernel on tcgen05 (head dim 64 or 128).
 struct PairTcArgs {
   PairSchedule sched;
@@ -42,6 +56,7 @@ struct PairTcArgs {
   float* cache_lse;   // [B, H, P, N]
   float scale_log2;   // softmax scale * log2(e)
   int* err;           // device error word
+  RopeQ rope;         // rotation applied to each Q tile after it lands in shared memory
 };
 cudaError_t launch_pair_tc(int d, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const PairTcArgs& args, int num_sms,

@@ -10,6 +10,8 @@
 //   warps 0-3  softmax warpgroup 0: query tile 0 (rows 0..127 of the unit), one row per thread
 //   warps 4-7  softmax warpgroup 1: query tile 1 (rows 128..255)
 //   warp  8    TMA producer: Q tiles per unit, then a ring of K and V tiles (128 rows each)
+//              (when RoPE is on, the softmax warpgroups rotate their Q tile in shared memory
+//              before the first Q K^T of the unit; K arrives already rotated)
 //   warp  9    MMA issuer: S_w = Q_w K^T (SS, both K-major) and O_w += P_w V (A from TMEM,
 //              V MN-major); owns the TMEM allocation
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d, 256+2d).
@@ -55,7 +57,7 @@ struct Cfg {
 
 template <int STAGES>
 struct SharedCtl {
-  uint64_t q_full, q_empty;
+  uint64_t q_full, q_ready, q_empty;  // Q landed / Q rotated (ready for the MMA) / Q consumed
   uint64_t kv_full[STAGES], kv_empty[STAGES];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t drained;
@@ -64,9 +66,16 @@ struct SharedCtl {
 };
 
 template <int D>
-constexpr int smem_bytes() {
-  return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::STAGES * Cfg<D>::TILE_BYTES +
-         (int)sizeof(SharedCtl<Cfg<D>::STAGES>);
+__host__ __device__ constexpr int ctl_bytes() {
+  return ((int)sizeof(SharedCtl<Cfg<D>::STAGES>) + 15) & ~15;
+}
+
+// Dynamic shared memory: 1 KB alignment slack, Q, the K/V ring, the control block, then the
+// RoPE table (rope_pairs (cos, sin) pairs; 0 without RoPE).
+template <int D>
+constexpr int smem_bytes(int rope_pairs) {
+  return 1024 + Cfg<D>::Q_BYTES + Cfg<D>::STAGES * Cfg<D>::TILE_BYTES + ctl_bytes<D>() +
+         8 * rope_pairs;
 }
 
 struct UnitInfo {
@@ -152,6 +161,100 @@ __device__ __forceinline__ void issue_qk(uint32_t d_t, uint32_t q_lo, uint32_t k
     mma_ss<1>(d_t, q_lo + kstep_off(k), hi, k_lo + kstep_off(k), hi, Cfg<D>::IDESC_QK);
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float2 ld_shared_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// Copies the RoPE table rows into shared memory as (cos, sin) pairs in the RopeQ layout. Run by
+// the `nthreads` threads with index `tid`; padding pairs are left unwritten (never read).
+__device__ __forceinline__ void stage_rope_table(const RopeQ& r, float2* tab, int tid, int nthreads) {
+  const int ht = r.dt >> 1, hh = r.dh >> 1, hw = r.dw >> 1;
+  const int nt_pairs = r.nT * r.sT, nh_pairs = r.Hl * r.sH;
+  for (int x = tid; x < r.n_pairs; x += nthreads) {
+    const float* c;
+    const float* sn;
+    int row, m, len;
+    if (x < nt_pairs) {
+      row = x / r.sT; m = x - row * r.sT; len = ht;
+      c = r.cos_t + (r.start_frame + row) * ht; sn = r.sin_t + (r.start_frame + row) * ht;
+    } else if (x < nt_pairs + nh_pairs) {
+      const int y = x - nt_pairs;
+      row = y / r.sH; m = y - row * r.sH; len = hh;
+      c = r.cos_h + row * hh; sn = r.sin_h + row * hh;
+    } else {
+      const int y = x - nt_pairs - nh_pairs;
+      row = y / r.sW; m = y - row * r.sW; len = hw;
+      c = r.cos_w + row * hw; sn = r.sin_w + row * hw;
+    }
+    if (m < len) tab[x] = make_float2(__ldg(c + m), __ldg(sn + m));
+  }
+}
+
+// Rotates one token's row of a Q tile in place in shared memory (3D RoPE keyed by the global
+// frame index; "Accelerating Video Generation Inference with Sequential-Parallel 3D Positional
+// Encoding Using a Global Time Index", section 2). The row is D bf16 values in 128-byte lines,
+// one per 64-channel chunk, with its 16-byte units stored at unit ^ (row mod 8). Channel pair
+// m = (2m, 2m+1) turns by the angle of table entry m of the token's frame (m < dt/2), row
+// (next dh/2) or column (last dw/2), evaluated as y0 = fl(fl(x0 c) - fl(x1 s)),
+// y1 = fl(fl(x0 s) + fl(x1 c)) with paired fp32 multiplies and adds (x0 c - x1 s is taken as
+// x0 c + x1 (-s): negation is exact), then rounded to bf16. n is the token's index in the
+// sequence; tab is the staged table (shared-space address).
+template <int D>
+__device__ __forceinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor, int n,
+                                             const RopeQ& r, uint32_t tab) {
+  const int hw_tokens = r.Hl * r.Wl;
+  const int tl = n / hw_tokens;
+  const int rem = n - tl * hw_tokens;
+  const int hp = rem / r.Wl;
+  const int wp = rem - hp * r.Wl;
+  const int ht = r.dt >> 1, hth = ht + (r.dh >> 1);
+  // byte addresses of pair 0 of each axis' row, offset so that pair m is at base + 8 m
+  const uint32_t bt = tab + 8u * static_cast<uint32_t>(tl * r.sT);
+  const uint32_t bh = tab + 8u * static_cast<uint32_t>(r.nT * r.sT + hp * r.sH - ht);
+  const uint32_t bw = tab + 8u * static_cast<uint32_t>(r.nT * r.sT + r.Hl * r.sH + wp * r.sW - hth);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint32_t addr = row_addr + c * kChunkBytes + ((x ^ row_xor) << 4);
+      const uint4 u = ld_shared_v4(addr);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int m = c * 32 + x * 4 + p;  // channel pair index
+        const uint32_t base = m < ht ? bt : (m < hth ? bh : bw);
+        const float2 cs = ld_shared_f2(base + 8u * m);
+        const float x0 = __uint_as_float(wv[p] << 16);
+        const float x1 = __uint_as_float(wv[p] & 0xFFFF0000u);
+        const float2 a = __fmul2_rn(make_float2(x0, x0), cs);                    // x0 c, x0 s
+        const float2 b = __fmul2_rn(make_float2(x1, x1), make_float2(-cs.y, cs.x));  // -x1 s, x1 c
+        const float2 y = __fadd2_rn(a, b);
+        o[p] = pack_bf16x2(y.x, y.y);
+      }
+      st_shared_v4(addr, o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     pair_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -164,6 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_smem = smem;
   uint8_t* kv_smem = smem + C::Q_BYTES;
   auto* ctl = reinterpret_cast<SharedCtl<STAGES>*>(kv_smem + STAGES * C::TILE_BYTES);
+  float2* rope_tab = reinterpret_cast<float2*>(kv_smem + STAGES * C::TILE_BYTES + ctl_bytes<D>());
+  const bool rope_on = args.rope.n_pairs > 0;
   volatile int* abort_w = &ctl->abort_word;
 
   const PairSchedule& sch = args.sched;
@@ -173,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ctl->abort_word = 0;
     mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_ready, 2 * kTileRows);
     mbar_init(&ctl->q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctl->kv_full[s], 1);
@@ -256,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_lo0 = sdesc_sw128_lo(smem_u32(kv_smem), kChunkBytes);  // LBO: next 64 ch
       for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x, ++uc) {
         const UnitInfo ui = decode_unit(sch, u);
-        ok = mbar_wait(&ctl->q_full, uc & 1u, abort_w);
+        ok = mbar_wait(rope_on ? &ctl->q_ready : &ctl->q_full, uc & 1u, abort_w);
         if (!ok) break;
         tc_fence_after_sync();
         // previous tile (for the P V product that trails each S = Q K^T by one tile)
@@ -310,9 +416,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_taddr = tbase + lane_base + C::s_col(w);
     const uint32_t o_taddr = tbase + lane_base + C::o_col(w);
     const float sl2 = args.scale_log2;
-    uint32_t g = 0;
+    // With RoPE on, the MMA issuer waits for q_ready instead of q_full: once the Q tiles of a
+    // unit have landed, each thread rotates its own row of its warpgroup's tile in place and
+    // arrives. For the first unit this happens up front; for each later one, right after the
+    // last P of the unit before (while the tensor core runs that unit's last P V), so that
+    // the next unit's first Q K^T overlaps this unit's epilogue.
+    const uint32_t q_row = smem_u32(q_smem) + w * C::TILE_BYTES + lrow * 128;
+    const uint32_t tab = smem_u32(rope_tab);
+    auto prepare_q = [&](int unit, uint32_t load) -> bool {
+      if (!warp_wait(&ctl->q_full, load & 1u, abort_w)) return false;
+      const int n_tok = decode_unit(sch, unit).row0 + w * kTileRows + lrow;
+      if (n_tok < args.N) rotate_q_row<D>(q_row, lrow & 7, n_tok, args.rope, tab);
+      fence_proxy_async_smem();
+      mbar_arrive(&ctl->q_ready);
+      return true;
+    };
+    uint32_t g = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x) {
+    if (rope_on) {
+      stage_rope_table(args.rope, rope_tab, threadIdx.x, 2 * kTileRows);
+      asm volatile("bar.sync 1, %0;" ::"n"(2 * kTileRows) : "memory");  // softmax warps only
+      if (blockIdx.x < sch.n_units) ok = prepare_q(blockIdx.x, 0);
+    }
+    for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x, ++uc) {
       const UnitInfo ui = decode_unit(sch, u);
       const int qrow = ui.qb * kUnitRows + w * kTileRows + lrow;  // row within partition i
       const bool row_ok = qrow < ui.n_i;
@@ -400,6 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
           tc_fence_before_sync();
           mbar_arrive(&ctl->p_full[w]);
+          if (rope_on && t == nt - 1 && (m & (m - 1)) == 0 &&
+              u + static_cast<int>(gridDim.x) < sch.n_units)
+            ok = prepare_q(u + gridDim.x, uc + 1);  // last P of the unit: hand over the next Q
         }
         if (!ok) break;
         // ---- epilogue of pair (i, j): O_ij = O / l, lse_ij = ln(l) + max
@@ -449,14 +578,17 @@ cudaError_t launch_pair_tc(int d, const CUtensorMap& mq, const CUtensorMap& mk, 
   if (args.sched.n_units <= 0) return cudaSuccess;
   const int grid = args.sched.n_units < num_sms ? args.sched.n_units : num_sms;
   cudaError_t err;
+  if (args.rope.n_pairs < 0 || 8 * args.rope.n_pairs > kRopeSmemMaxBytes) return cudaErrorInvalidValue;
   if (d == 128) {
-    constexpr int smem = smem_bytes<128>();
-    err = cudaFuncSetAttribute(pair_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = smem_bytes<128>(args.rope.n_pairs);
+    err = cudaFuncSetAttribute(pair_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem_bytes<128>(kRopeSmemMaxBytes / 8));
     if (err != cudaSuccess) return err;
     pair_tc_kernel<128><<<grid, kThreads, smem, stream>>>(mq, mk, mv, args);
   } else if (d == 64) {
-    constexpr int smem = smem_bytes<64>();
-    err = cudaFuncSetAttribute(pair_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = smem_bytes<64>(args.rope.n_pairs);
+    err = cudaFuncSetAttribute(pair_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem_bytes<64>(kRopeSmemMaxBytes / 8));
     if (err != cudaSuccess) return err;
     pair_tc_kernel<64><<<grid, kThreads, smem, stream>>>(mq, mk, mv, args);
   } else {

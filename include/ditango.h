@@ -167,7 +167,9 @@ int ditango_plan_set_profile_events(ditango_plan_t plan, void* const* events);
  * out: [B, N, H, d], same dtype as q, d contiguous. out_lse: [B, H, N] F32, or NULL.
  * softmax_scale: the `scale` of the pair-state definition (commonly 1/sqrt(d)).
  * workspace: device memory of at least ditango_attn_step_workspace_size(...) bytes, 256-byte
- *   aligned (may be NULL when that size is 0). Its contents need not be preserved.
+ *   aligned (may be NULL when that size is 0). Its contents need not be preserved. It holds
+ *   the rotated k, and the rotated q unless the BF16 pair kernel rotates each Q tile itself
+ *   (it does when the table rows of the sequence, as (cos, sin) pairs, fit in 32 KB).
  * On success the computed pairs are recorded in the plan as valid at this step. The result
  * is complete when the stream reaches this point. Kernel-side barrier timeouts are reported
  * by ditango_device_status, not here. */

@@ -52,6 +52,23 @@ def test_long_720p_like_reduced_all_rows():
     run_all_steps(ParityRun(w))
 
 
+def test_rope_d64_even_table_halves():
+    # d = 64: 12/10/10 channel pairs per axis (even halves, padded to odd strides in the
+    # shared-memory table), 4 frames from global frame 3, Q tiles spanning frame boundaries
+    w = wl.scaled(wl.get("small_bf16"), "small_rope", H=2, T=4, Hl=8, Wl=24, start_frame=3,
+                  steps=4)
+    w.rope = True
+    run_all_steps(ParityRun(w))
+
+
+def test_rope_tables_too_large_for_shared_memory():
+    # a 2 x 1000 latent needs 1000 w rows of 21 pairs: more than the pair kernel stages in shared
+    # memory, so Q goes through the rotary pre-pass with K
+    w = wl.scaled(wl.get("wan14b_layer"), "wide_rope", H=2, T=1, Hl=2, Wl=1000, start_frame=1,
+                  steps=2)
+    run_all_steps(ParityRun(w))
+
+
 @pytest.mark.parametrize("P,N,d", [(1, 300, 128), (1, 700, 64), (64, 64 * 3 + 5, 128),
                                    (64, 64, 64), (3, 129, 128), (5, 1000, 64)])
 def test_edge_partitions(P, N, d):
