@@ -17,8 +17,16 @@
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d, 256+2d).
 // P_w overwrites the first 64 columns of S_w as packed bf16; tcgen05.mma operations issued by
 // one thread execute in order, so S_w of the next tile is written only after P_w is consumed.
-// The online softmax keeps a stale running max until the new tile max exceeds it by more than
-// 2^8 (values of P then stay below 256); only then are O and the row sum rescaled.
+// The MMA warp runs its loop converged and lets one elected lane issue (see mma_ss in
+// ptx_sm103.cuh).
+// Online softmax with a lazily updated reference m: the first tile of a partition takes its
+// exact row max; later tiles reuse m and check only the row sum of their exponentials, and a
+// row whose tile sum exceeds 2^8 (a score above the reference by up to 8 in log2 units, or
+// many close to it) takes the exact max of that tile, rescales O and l, and recomputes P.
+// The result does not depend on m mathematically; numerically, a reference at the exact max
+// makes the largest term of a row exactly 1 in bf16, which keeps the bf16 rounding of P from
+// reaching the largest products (measured: letting P grow to 2^12 or beyond roughly doubled
+// the worst output error on head-scaled inputs).
 // Every barrier wait is bounded (see ptx_sm103.cuh); a timeout makes all roles stop, drain
 // their copies, free TMEM and record an error code.
 #include <cuda_bf16.h>
@@ -39,7 +47,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kTileRows = 128;               // query rows per tile == KV rows per tile
 constexpr int kUnitRows = 2 * kTileRows;     // query rows per unit
 constexpr int kChunkBytes = 128 * 128;       // 128 rows x 64 bf16 (one swizzle-atom column)
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleSum = 256.0f;  // tile row sum above which m moves to the exact max
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
@@ -119,6 +127,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // the epilogue of the previous partition to have read O_w (first tile of a partition), and
 // for the V tile; then eight K=16 steps with A read from TMEM (P) and B = V (MN-major).
 // v_lo0 is the low descriptor half of ring slot 0 for an MN-major operand.
+// Run by the whole MMA warp (converged); one elected lane issues.
 template <int D>
 __device__ __forceinline__ bool issue_pv(SharedCtl<Cfg<D>::STAGES>* ctl, int w, uint32_t prev_g,
                                          uint32_t prev_v, uint32_t prev_pidx, bool prev_first,
@@ -126,10 +135,10 @@ __device__ __forceinline__ bool issue_pv(SharedCtl<Cfg<D>::STAGES>* ctl, int w, 
                                          volatile int* abort_w) {
   using C = Cfg<D>;
   constexpr int STAGES = C::STAGES;
-  if (!mbar_wait(&ctl->p_full[w], prev_g & 1u, abort_w)) return false;
-  if (prev_first && prev_pidx >= 1 && !mbar_wait(&ctl->o_free[w], (prev_pidx - 1) & 1u, abort_w))
+  if (!warp_wait(&ctl->p_full[w], prev_g & 1u, abort_w)) return false;
+  if (prev_first && prev_pidx >= 1 && !warp_wait(&ctl->o_free[w], (prev_pidx - 1) & 1u, abort_w))
     return false;
-  if (w == 0 && !mbar_wait(&ctl->kv_full[prev_v % STAGES], (prev_v / STAGES) & 1u, abort_w))
+  if (w == 0 && !warp_wait(&ctl->kv_full[prev_v % STAGES], (prev_v / STAGES) & 1u, abort_w))
     return false;
   tc_fence_after_sync();
   const uint32_t v_lo = v_lo0 + (prev_v % STAGES) * (C::TILE_BYTES >> 4);
@@ -154,7 +163,8 @@ __host__ __device__ constexpr uint32_t kstep_off(int k) {
 
 // S_w = Q_w K^T for the K tile at low descriptor half k_lo: D/16 steps, both operands K-major.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_t, uint32_t q_lo, uint32_t k_lo, uint32_t hi) {
+__device__ __forceinline__ void issue_qk(uint32_t d_t, uint32_t q_lo, uint32_t k_lo,
+                                         uint32_t hi) {
   mma_ss<0>(d_t, q_lo, hi, k_lo, hi, Cfg<D>::IDESC_QK);
 #pragma unroll
   for (int k = 1; k < D / 16; ++k)
@@ -214,9 +224,9 @@ __device__ __forceinline__ void stage_rope_table(const RopeQ& r, float2* tab, in
 // one per 64-channel chunk, with its 16-byte units stored at unit ^ (row mod 8). Channel pair
 // m = (2m, 2m+1) turns by the angle of table entry m of the token's frame (m < dt/2), row
 // (next dh/2) or column (last dw/2), evaluated as y0 = fl(fl(x0 c) - fl(x1 s)),
-// y1 = fl(fl(x0 s) + fl(x1 c)) with paired fp32 multiplies and adds (x0 c - x1 s is taken as
-// x0 c + x1 (-s): negation is exact), then rounded to bf16. n is the token's index in the
-// sequence; tab is the staged table (shared-space address).
+// y1 = fl(fl(x0 s) + fl(x1 c)) with fp32 multiplies and adds that are never contracted into
+// FMAs (the rotary pre-pass evaluates the same expression), then rounded to bf16. n is the
+// token's index in the sequence; tab is the staged table (shared-space address).
 template <int D>
 __device__ __forceinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor, int n,
                                              const RopeQ& r, uint32_t tab) {
@@ -245,13 +255,59 @@ __device__ __forceinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor
         const float2 cs = ld_shared_f2(base + 8u * m);
         const float x0 = __uint_as_float(wv[p] << 16);
         const float x1 = __uint_as_float(wv[p] & 0xFFFF0000u);
-        const float2 a = __fmul2_rn(make_float2(x0, x0), cs);                    // x0 c, x0 s
-        const float2 b = __fmul2_rn(make_float2(x1, x1), make_float2(-cs.y, cs.x));  // -x1 s, x1 c
-        const float2 y = __fadd2_rn(a, b);
-        o[p] = pack_bf16x2(y.x, y.y);
+        const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+        const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+        o[p] = pack_bf16x2(y0, y1);
       }
       st_shared_v4(addr, o[0], o[1], o[2], o[3]);
     }
+  }
+}
+
+// P = 2^(s * scale_log2 - m) for one row of a 128-key tile, packed to bf16 pairs in pk;
+// returns the row sum of the fp32 values. Paired fp32 FMA/add instructions halve the ALU issue
+// of the scale-subtract and of the sum (four independent pair sums); the exponentials go to the
+// SFU.
+__device__ __forceinline__ float exp_pack_p(const float (&s)[kTileRows], float sl2, float m,
+                                            uint32_t (&pk)[kTileRows / 2]) {
+  const float2 sl2x2 = make_float2(sl2, sl2);
+  const float2 negm2 = make_float2(-m, -m);
+  float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                  make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int c = 0; c < kTileRows / 2; ++c) {
+    const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, negm2);
+    const float p0 = ex2_approx(x.x);
+    const float p1 = ex2_approx(x.y);
+    l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
+    pk[c] = pack_bf16x2(p0, p1);
+  }
+  const float2 l2 = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
+  return l2.x + l2.y;
+}
+
+// Row max of a tile: eight independent three-input max chains, then a short tree.
+__device__ __forceinline__ float tile_max(const float (&s)[kTileRows]) {
+  float m8[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) m8[x] = fmaxf(s[x], s[8 + x]);
+#pragma unroll
+  for (int c = 16; c < kTileRows; c += 16)
+#pragma unroll
+    for (int x = 0; x < 8; ++x) m8[x] = fmax3(m8[x], s[c + x], s[c + 8 + x]);
+  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
+// Reads S (one row of 128 fp32 scores per thread) from TMEM; keys at or past `valid` get -inf.
+__device__ __forceinline__ void load_s(uint32_t s_taddr, int valid, float (&s)[kTileRows]) {
+  uint32_t r[kTileRows];
+  tmem_ld_32x32b_x128(s_taddr, r);
+#pragma unroll
+  for (int c = 0; c < kTileRows; ++c) s[c] = __uint_as_float(r[c]);
+  if (valid < kTileRows) {
+#pragma unroll
+    for (int c = 0; c < kTileRows; ++c)
+      if (c >= valid) s[c] = -INFINITY;
   }
 }
 
@@ -352,7 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (converged, waits made warp-uniform); one elected lane
+    // issues every MMA and commit.
+    {
       uint32_t e = 0, uc = 0, g = 0, pidx = 0;
       bool ok = true;
       const uint32_t desc_hi = sdesc_sw128_hi(1024);  // SBO: 8 rows of 128 bytes
@@ -362,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_lo0 = sdesc_sw128_lo(smem_u32(kv_smem), kChunkBytes);  // LBO: next 64 ch
       for (int u = blockIdx.x; ok && u < sch.n_units; u += gridDim.x, ++uc) {
         const UnitInfo ui = decode_unit(sch, u);
-        ok = mbar_wait(rope_on ? &ctl->q_ready : &ctl->q_full, uc & 1u, abort_w);
+        ok = warp_wait(rope_on ? &ctl->q_ready : &ctl->q_full, uc & 1u, abort_w);
         if (!ok) break;
         tc_fence_after_sync();
         // previous tile (for the P V product that trails each S = Q K^T by one tile)
@@ -373,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nt = ntiles_of(sch, j);
           for (int t = 0; t < nt; ++t, e += 2, ++g) {
             const uint32_t ke = e;
-            ok = mbar_wait(&ctl->kv_full[ke % STAGES], (ke / STAGES) & 1u, abort_w);
+            ok = warp_wait(&ctl->kv_full[ke % STAGES], (ke / STAGES) & 1u, abort_w);
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t k_lo = k_lo0 + (ke % STAGES) * (C::TILE_BYTES >> 4);
@@ -446,47 +504,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = __ffsll(static_cast<long long>(m)) - 1;
         const int nj = sch.offsets[j + 1] - sch.offsets[j];
         const int nt = (nj + kTileRows - 1) / kTileRows;
-        float m_run = -FLT_MAX, l_run = 0.f;
+        float m_run = 0.f, l_run = 0.f;  // reference (log2 units) and row sum of the partition
         for (int t = 0; t < nt; ++t, ++g) {
           ok = warp_wait(&ctl->s_full[w], g & 1u, abort_w);
           if (!ok) break;
           tc_fence_after_sync();
-          float s[kTileRows];
-          {
-            uint32_t r[kTileRows];
-            tmem_ld_32x32b_x128(s_taddr, r);
-#pragma unroll
-            for (int c = 0; c < kTileRows; ++c) s[c] = __uint_as_float(r[c]);
-          }
           const int valid = nj - t * kTileRows;
-          if (valid < kTileRows) {
-#pragma unroll
-            for (int c = 0; c < kTileRows; ++c)
-              if (c >= valid) s[c] = -INFINITY;
-          }
-          // row max: eight independent three-input max chains, then a short tree
-          float m8[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x) m8[x] = fmaxf(s[x], s[8 + x]);
-#pragma unroll
-          for (int c = 16; c < kTileRows; c += 16)
-#pragma unroll
-            for (int x = 0; x < 8; ++x) m8[x] = fmax3(m8[x], s[c + x], s[c + 8 + x]);
-          const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                                 fmaxf(m8[6], m8[7]));
-          const float m_tile = mx * sl2;
-          bool need_rescale = false;
-          float alpha = 1.f;
-          if (t == 0) {
-            m_run = m_tile;
-            l_run = 0.f;
-          } else if (m_tile > m_run + kRescaleLog2) {
-            alpha = ex2_approx(m_run - m_tile);
-            m_run = m_tile;
-            l_run *= alpha;
-            need_rescale = true;
-          }
-          if (__any_sync(0xffffffffu, need_rescale)) {
+          float s[kTileRows];
+          load_s(s_taddr, valid, s);
+          if (t == 0) m_run = tile_max(s) * sl2;  // first tile of the partition: exact max
+          uint32_t pk[kTileRows / 2];
+          float l_t = exp_pack_p(s, sl2, m_run, pk);
+          const bool redo = t > 0 && !(l_t <= kRescaleSum);
+          if (__any_sync(0xffffffffu, redo)) {
+            // the rows whose sum left the range move m to the exact max of this tile (S is
+            // re-read: it is still intact in TMEM), rescale O and l, and recompute P
+            load_s(s_taddr, valid, s);
+            const float m_tile = tile_max(s) * sl2;
+            float alpha = 1.f;
+            if (redo) {
+              const float m_new = fmaxf(m_run, m_tile);
+              alpha = ex2_approx(m_run - m_new);
+              l_run *= alpha;
+              m_run = m_new;
+            }
             // O holds the sum over earlier tiles of this partition: wait for the last P V
             ok = warp_wait(&ctl->o_done[w], (g - 1) & 1u, abort_w);
             if (!ok) break;
@@ -499,30 +540,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
               tmem_st_32x32b_x32(o_taddr + c * 32, r);
             }
+            l_t = exp_pack_p(s, sl2, m_run, pk);
           }
-          // p = 2^(s * scale * log2(e) - m): paired fp32 FMA/add instructions halve the ALU
-          // issue of the scale-subtract and of the row sum (four independent pair sums); the
-          // exponentials go to the SFU, which competes far less with tensor-core issue
-          const float2 sl2x2 = make_float2(sl2, sl2);
-          const float2 negm2 = make_float2(-m_run, -m_run);
-          float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
+          {
+            uint32_t lo[32], hi[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const int e0 = 64 * half + 2 * c;
-              const float2 x = __ffma2_rn(make_float2(s[e0], s[e0 + 1]), sl2x2, negm2);
-              const float p0 = ex2_approx(x.x);
-              const float p1 = ex2_approx(x.y);
-              l4[c & 3] = __fadd2_rn(l4[c & 3], make_float2(p0, p1));
-              pk[c] = pack_bf16x2(p0, p1);
+              lo[c] = pk[c];
+              hi[c] = pk[32 + c];
             }
-            tmem_st_32x32b_x32(s_taddr + 32 * half, pk);
+            tmem_st_32x32b_x32(s_taddr, lo);
+            tmem_st_32x32b_x32(s_taddr + 32, hi);
           }
-          const float2 l2 = __fadd2_rn(__fadd2_rn(l4[0], l4[1]), __fadd2_rn(l4[2], l4[3]));
-          l_run += l2.x + l2.y;
+          l_run = t == 0 ? l_t : l_run + l_t;
           tmem_st_wait();
           tc_fence_before_sync();
           mbar_arrive(&ctl->p_full[w]);
@@ -531,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = prepare_q(u + gridDim.x, uc + 1);  // last P of the unit: hand over the next Q
         }
         if (!ok) break;
-        // ---- epilogue of pair (i, j): O_ij = O / l, lse_ij = ln(l) + max
+        // ---- epilogue of pair (i, j): O_ij = O / l, lse_ij = ln 2 * (m_run + log2 l)
         ok = warp_wait(&ctl->o_done[w], (g - 1) & 1u, abort_w);
         if (!ok) break;
         tc_fence_after_sync();

@@ -138,36 +138,15 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrives once on the mbarrier when every tcgen05.mma issued so far by this thread has
-// completed.
+// Arrives once on the mbarrier when every tcgen05.mma issued so far by the issuing thread has
+// completed. Warp-converged: every lane calls it and the lane chosen by elect.sync (the same
+// lane that issues the MMAs, see mma_ss) executes it.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// ---------------------------------------------------------------------------------------
-// tcgen05.mma, kind::f16 (bf16 x bf16 -> fp32 accumulate in TMEM), single CTA
-// ---------------------------------------------------------------------------------------
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -210,28 +189,36 @@ __host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo_bytes) {
   return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
-// tcgen05.mma with descriptors given as halves and the accumulate flag fixed at compile time,
-// so that issuing one MMA costs a handful of instructions (a single issuing thread has to keep
-// the tensor pipe fed at one 128x128x16 MMA every ~64 cycles).
+// tcgen05.mma, kind::f16 (bf16 x bf16 -> fp32 accumulate in TMEM), single CTA, with the
+// descriptors given as 32-bit halves and the accumulate flag fixed at compile time, so that one
+// MMA costs a handful of instructions (the tensor pipe takes a 128x128x16 MMA every ~64
+// cycles). Warp-converged: every lane of the issuing warp makes the call with the same
+// operands, and the lane chosen by elect.sync over the full warp issues. Measured on GB300
+// with softmax-like warps busy on the same SM sub-partition: this form kept the pipe at full
+// rate, while the same loop run by one lane (or converged but predicated on a lane-index test)
+// reached 45-60% of it.
 template <int ACC>
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
-                                       uint32_t b_hi, uint32_t idesc) {
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                       uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem desc]
 template <int ACC>
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                        uint32_t b_hi, uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "mov.b64 db, {%2, %3};\n\t"
       "setp.ne.b32 p, %5, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
       : "memory");
 }
