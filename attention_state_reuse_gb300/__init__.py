@@ -31,7 +31,7 @@ STATUS = {
 SYMBOLS = [
     "ditango_plan", "ditango_plan_destroy", "ditango_plan_set_mask", "ditango_plan_check_mask",
     "ditango_plan_get_offsets", "ditango_plan_get_pairs", "ditango_plan_get_cache_state",
-    "ditango_plan_set_profile_events",
+    "ditango_plan_set_profile_events", "ditango_plan_inject_fault",
     "ditango_attn_step", "ditango_attn_step_static_workspace",
     "ditango_attn_step_workspace_size", "ditango_merge",
     "ditango_rope_build_tables", "ditango_device_status", "ditango_status_string",
@@ -92,6 +92,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ditango_plan_get_pairs.argtypes = [vp, u8p, P(i32), P(i32)]
     lib.ditango_plan_get_cache_state.argtypes = [vp, u8p, P(i64), P(i64)]
     lib.ditango_plan_set_profile_events.argtypes = [vp, P(vp)]
+    lib.ditango_plan_inject_fault.argtypes = [vp, ctypes.c_int32]
     lib.ditango_attn_step.argtypes = [vp, P(Tensor), P(Tensor), P(Tensor), P(Rope), u8p,
                                       P(StateCache), P(Tensor), P(Tensor), ctypes.c_float, vp,
                                       ctypes.c_size_t, vp]
@@ -224,6 +225,10 @@ class Plan:
     def set_mask(self, mask):
         arr, ptr = _mask_ptr(mask, self.P)
         _check(_lib().ditango_plan_set_mask(self._h, ptr), "ditango_plan_set_mask")
+
+    def inject_fault(self, kind=1):
+        """Arms (1) or disarms (0) the one-shot device-timeout test fault of the next bf16 step."""
+        _check(_lib().ditango_plan_inject_fault(self._h, int(kind)), "ditango_plan_inject_fault")
 
     def set_profile_events(self, events):
         """Four torch.cuda.Event(enable_timing=True) recorded around the step's kernels, or None."""

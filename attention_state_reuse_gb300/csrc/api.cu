@@ -279,6 +279,8 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     pa.scale_log2 = softmax_scale * 1.4426950408889634f;
     pa.err = dev->err_ptr;
     pa.rope = rq;
+    pa.inject_fault = plan->inject_fault;
+    plan->inject_fault = 0;
     if (launch_pair_tc(static_cast<int>(d), mq, mk, mv, pa, dev->num_sms, s) != cudaSuccess)
       return DITANGO_ERR_CUDA;
   } else {

@@ -57,6 +57,7 @@ struct PairTcArgs {
   float scale_log2;   // softmax scale * log2(e)
   int* err;           // device error word
   RopeQ rope;         // rotation applied to each Q tile after it lands in shared memory
+  int32_t inject_fault;  // 1: CTA 0 skips the copy of its first K tile (test hook)
 };
 cudaError_t launch_pair_tc(int d, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const PairTcArgs& args, int num_sms,

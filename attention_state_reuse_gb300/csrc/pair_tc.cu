@@ -389,6 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(&ctl->kv_empty[slot], ((e / STAGES) - 1) & 1u, abort_w);
                 if (!ok) break;
               }
+              // test hook: the first K tile of CTA 0 never arrives, so the MMA warp's bounded
+              // wait for it runs out and the CTA takes its abort path
+              if (args.inject_fault && blockIdx.x == 0 && e == 0) continue;
               mbar_arrive_expect_tx(&ctl->kv_full[slot], C::TILE_BYTES);
               const CUtensorMap* mp = kind == 0 ? &map_k : &map_v;
               for (int c = 0; c < C::CH; ++c)

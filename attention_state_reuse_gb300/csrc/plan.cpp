@@ -160,6 +160,12 @@ int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pa
   return DITANGO_OK;
 }
 
+int ditango_plan_inject_fault(ditango_plan_t plan, int32_t kind) {
+  if (plan == nullptr || kind < 0 || kind > 1) return DITANGO_ERR_INVALID_ARG;
+  plan->inject_fault = kind;
+  return DITANGO_OK;
+}
+
 int ditango_plan_set_profile_events(ditango_plan_t plan, void* const* events) {
   if (plan == nullptr) return DITANGO_ERR_INVALID_ARG;
   if (events == nullptr) {

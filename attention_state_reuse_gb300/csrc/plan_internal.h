@@ -15,6 +15,7 @@ struct ditango_plan_s {
   int64_t steps = 0;                  // steps run so far
   void* events[4] = {nullptr, nullptr, nullptr, nullptr};  // optional timing hook
   bool profile = false;
+  int32_t inject_fault = 0;  // one-shot test hook for the next bf16 pair kernel (0 = none)
 };
 
 namespace ditango {

@@ -153,6 +153,18 @@ int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* s
  * stream, so that the caller can read per-kernel device time with cudaEventElapsedTime. */
 int ditango_plan_set_profile_events(ditango_plan_t plan, void* const* events);
 
+/* ---- fault injection (a test hook; the paper has no counterpart) ------------------------
+ * kind 1 arms a one-shot fault for the next ditango_attn_step on this plan that runs the BF16
+ * pair kernel; kind 0 disarms. In that launch the first CTA skips the copy of its first K tile,
+ * so the MMA warp's bounded wait for it runs out after about one second: every role of that CTA
+ * stops, waits (bounded) for its copies and MMAs in flight, frees its TMEM and sets the device
+ * error word. The step itself returns DITANGO_OK (the fault happens on the device);
+ * ditango_device_status then reports DITANGO_ERR_DEVICE_TIMEOUT. The outputs of that step and
+ * the cache slots of the aborted CTA's work are unspecified; the context stays usable, and a
+ * following step that computes every pair restores the cache. Nothing traps, faults or hangs.
+ * Errors: DITANGO_ERR_INVALID_ARG for a NULL plan or another kind. */
+int ditango_plan_inject_fault(ditango_plan_t plan, int32_t kind);
+
 /* ---- one attention-layer step -----------------------------------------------------------
  * Source: DiTango, Methodology 1-2 (compute or reuse per pair, then compose the states);
  * rotary prologue from the Causal-RoPE SP page, section 2.

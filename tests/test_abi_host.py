@@ -84,6 +84,16 @@ def test_plan_rejects_bad_arguments(ditango):
     assert e.value.name == "INVALID_MASK"
 
 
+def test_fault_injection_arguments(ditango):
+    plan = ditango.Plan(100, 4)
+    plan.inject_fault(1)
+    plan.inject_fault(0)
+    for kind in (2, -1):
+        with pytest.raises(ditango.DitangoError) as e:
+            plan.inject_fault(kind)
+        assert e.value.name == "INVALID_ARG"
+
+
 def test_mask_checks_match_oracle_book(ditango):
     P = 8
     plan = ditango.Plan(4096, P)
