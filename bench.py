@@ -5,8 +5,8 @@ Workload (default): the Wan2.1-14B-shaped layer - B=1, H=40, d=128, bf16, N=3276
 (21x30x52 latent), P=8 contiguous partitions, 3D RoPE (t/h/w split 44/42/42) with a global
 time index, per-head input scales U(0.5, 2); the timed step reuses every pair with |i-j| >= 2
 (42 of 64 pairs) after an all-compute anchor step filled the state cache. A step is one call
-of ditango_attn_step: RoPE of q and k, fresh states of the 22 computed pairs, merge of all
-8 states of every row. Inputs are synthetic (seeded) and resident in HBM before timing;
+of ditango_attn_step: RoPE of k (q is rotated inside the pair kernel), fresh states of the 22
+computed pairs, merge of all 8 states of every row. Inputs are synthetic (seeded) and resident in HBM before timing;
 they are larger than L2 (335 MB per tensor), so no L2 flush is needed between steps.
 
 Prints one JSON line: ms per step (lower is better) plus effective TFLOP/s counted over
@@ -279,7 +279,7 @@ def run_ours(args, w, rank, world):
                    "latent": [w.T, w.Hl, w.Wl], "rope": w.rope, "reuse_mask": f"|i-j|>={w.schedule[1][1]}" if w.schedule[1][0] == "dist" else w.schedule[1][0],
                    "reuse_fraction": round(float(np.asarray(mask).mean()), 4),
                    "l2": "inputs larger than L2 (335 MB per tensor); no flush"},
-        "effective_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "effective_tflops": round(world * flops / (ms * 1e-3) / 1e12, 2),  # all ranks
         "pair_flops_per_step": flops,
         "kernel_ms": {"rope": round(rope_ms, 4), "pair": round(pair_ms, 4),
                       "merge": round(merge_ms, 4)},
@@ -297,7 +297,7 @@ def run_ours(args, w, rank, world):
                            "bytes_per_launch": mbytes},
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": K * (3 if w.rope else 2),
+        "gpu_launches": world * K * (3 if w.rope else 2),  # all ranks
         "reuse_sweep": sweep,
         "clocks": ck,
     }
@@ -385,14 +385,26 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest of every rank's x (a timing), on the process group's own device."""
     if world <= 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_workload(w, rank):
+    """Rank r runs its own replica of the layer: same shapes, inputs seeded from config index
+    c + 100 r (weak scaling; no data crosses ranks)."""
+    import copy
+
+    r = copy.deepcopy(w)
+    r.index += 100 * rank
+    return r
 
 
 # ------------------------------------------------------------------------------ CPU oracle
@@ -532,10 +544,10 @@ def main():
 
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-        w.index += 100 * rank  # each rank runs its own replica of the layer (weak scaling)
+        w = replica_workload(w, rank)
     line = run_ours(args, w, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:
             base = OracleBaseline(w, args.cpu_budget)
             est_ms, spent = base.estimate_ms()
             line["cpu_baseline"] = {"value": round(est_ms, 1), "unit": "ms",
