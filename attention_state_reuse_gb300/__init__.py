@@ -15,7 +15,7 @@ from ._build import LIB_PATH, build  # noqa: F401  (re-exported for users who bu
 
 __all__ = [
     "DitangoError", "Plan", "attn_step", "merge", "workspace_size", "RopeTables",
-    "device_status", "new_state_cache", "load_library", "SYMBOLS",
+    "device_status", "new_state_cache", "new_group_state", "load_library", "SYMBOLS",
 ]
 
 F32, BF16 = 0, 1
@@ -52,7 +52,15 @@ class Tensor(ctypes.Structure):
 
 
 class StateCache(ctypes.Structure):
-    _fields_ = [("O", Tensor), ("lse", Tensor)]
+    _fields_ = [("O", Tensor), ("lse", Tensor), ("group_O", Tensor), ("group_lse", Tensor)]
+
+
+def _state_cache(cache_O, cache_lse, group):
+    c = StateCache(tensor_desc(cache_O), tensor_desc(cache_lse))
+    if group is not None:
+        c.group_O = tensor_desc(group[0])
+        c.group_lse = tensor_desc(group[1])
+    return c
 
 
 class Rope(ctypes.Structure):
@@ -253,6 +261,16 @@ def new_state_cache(B, H, P, N, d, dtype, device="cuda"):
     return O, lse
 
 
+def new_group_state(B, H, N, d, device="cuda"):
+    """Allocates the optional group states of a cache: O [B, H, N, d] and lse [B, H, N], fp32.
+    Pass them as `group=` to attn_step with the same plan every step."""
+    import torch
+
+    O = torch.empty((B, H, N, d), dtype=torch.float32, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    return O, lse
+
+
 def workspace_size(plan: Plan, B: int, H: int, d: int, dtype, use_rope: bool) -> int:
     import torch
 
@@ -294,12 +312,13 @@ class RopeTables:
 
 def attn_step(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None, reuse_mask=None,
               rope: RopeTables | None = None, softmax_scale: float | None = None, workspace=None,
-              stream=None) -> None:
-    """One attention-layer step (ditango_attn_step), asynchronous on `stream`."""
+              stream=None, group=None) -> None:
+    """One attention-layer step (ditango_attn_step), asynchronous on `stream`. `group`: the
+    cache's optional group states (new_group_state), or None."""
     if softmax_scale is None:
         softmax_scale = q.shape[-1] ** -0.5
     qd, kd, vd, od = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
-    cache = StateCache(tensor_desc(cache_O), tensor_desc(cache_lse))
+    cache = _state_cache(cache_O, cache_lse, group)
     ld = tensor_desc(out_lse) if out_lse is not None else None
     rs = rope.struct() if rope is not None else None
     arr, mptr = _mask_ptr(reuse_mask, plan.P)
@@ -315,14 +334,15 @@ def attn_step(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None, reuse_
 
 def attn_step_static_workspace(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None,
                                reuse_mask=None, rope: RopeTables | None = None,
-                               softmax_scale: float | None = None, stream=None) -> None:
+                               softmax_scale: float | None = None, stream=None,
+                               group=None) -> None:
     """ditango_attn_step_static_workspace: the step without a caller workspace, for callers
     that cannot allocate device memory; its scratch lives in a 64 MiB array inside the
     library (steps needing more are refused with WORKSPACE). Concurrent calls race on it."""
     if softmax_scale is None:
         softmax_scale = q.shape[-1] ** -0.5
     qd, kd, vd, od = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
-    cache = StateCache(tensor_desc(cache_O), tensor_desc(cache_lse))
+    cache = _state_cache(cache_O, cache_lse, group)
     ld = tensor_desc(out_lse) if out_lse is not None else None
     rs = rope.struct() if rope is not None else None
     arr, mptr = _mask_ptr(reuse_mask, plan.P)

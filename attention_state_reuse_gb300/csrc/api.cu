@@ -6,7 +6,8 @@
 //      the pair kernel rotates each Q tile in shared memory after loading it (pair_tc.cu);
 //   3. fresh states for the computed pairs only, written into the state cache (pair_tc.cu for
 //      bf16, pair_f32.cu for fp32), over a schedule that lists computed pairs only;
-//   4. merge of all P cached states of every query row (merge.cu);
+//   4. merge of every query row's states (merge.cu): its computed states with its reused
+//      ones, or with one group state per row composed from them (rebuilt when stale);
 //   5. record the computed pairs as valid at this step.
 // Every device buffer belongs to the caller; nothing here allocates device memory.
 #include <cudaTypedefs.h>
@@ -186,6 +187,20 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
       cL.shape[3] != N || !contiguous(&cL))
     return DITANGO_ERR_SHAPE;
   if (!aligned16(cO.ptr) || !aligned16(cL.ptr)) return DITANGO_ERR_ALIGN;
+  const ditango_tensor& gO = cache->group_O;
+  const ditango_tensor& gL = cache->group_lse;
+  const bool use_group = gO.ptr != nullptr;
+  if ((gO.ptr == nullptr) != (gL.ptr == nullptr)) return DITANGO_ERR_INVALID_ARG;
+  if (use_group) {
+    if (gO.dtype != DITANGO_F32 || gL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+    if (gO.ndim != 4 || gO.shape[0] != B || gO.shape[1] != H || gO.shape[2] != N ||
+        gO.shape[3] != d || !contiguous(&gO))
+      return DITANGO_ERR_SHAPE;
+    if (gL.ndim != 3 || gL.shape[0] != B || gL.shape[1] != H || gL.shape[2] != N ||
+        !contiguous(&gL))
+      return DITANGO_ERR_SHAPE;
+    if (!aligned16(gO.ptr) || !aligned16(gL.ptr)) return DITANGO_ERR_ALIGN;
+  }
   if (rope != nullptr) {
     if ((st = check_rope(rope, N, d)) != DITANGO_OK) return st;
     const size_t need = rope_workspace_bytes(B, N, H, d, dtype);
@@ -301,29 +316,70 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     if (launch_pair_f32(static_cast<int>(d), pa, s) != cudaSuccess) return DITANGO_ERR_CUDA;
   }
 
-  // ---- 3. merge every row's P states (cache layout [B, H, P, N, d])
+  // ---- 3. merge: each row's computed states with its reused ones, or with the group state of
+  // its partition's reused pairs (built first where it is missing or out of date)
   if (!mark(2)) return DITANGO_ERR_CUDA;
-  MergeArgs ma;
+  const size_t esz = elem_size(dtype);
+  uint64_t reused[kMaxP] = {}, rebuild = 0;
+  for (int32_t i = 0; i < P; ++i) {
+    reused[i] = plan_reused_set(plan, reuse_mask, i);
+    if (use_group && reused[i] != 0 && !plan_group_current(plan, gO.ptr, i, reused[i]))
+      rebuild |= uint64_t{1} << i;
+  }
+  for (uint64_t m = rebuild; m; m &= m - 1) {
+    const int32_t i = __builtin_ctzll(m);
+    plan->group_set[i] = 0;  // invalid until this build has been launched
+    const int64_t off = plan->offsets[i];
+    MergeArgs ga;
+    std::memset(&ga, 0, sizeof(ga));
+    ga.d = static_cast<int32_t>(d);
+    ga.dtype = dtype;
+    ga.out_dtype = DITANGO_F32;
+    ga.G1 = B; ga.G2 = H; ga.R = plan->offsets[i + 1] - off;
+    for (uint64_t r = reused[i]; r; r &= r - 1) {
+      const int32_t j = __builtin_ctzll(r);
+      ga.O[ga.n] = static_cast<const uint8_t*>(cO.ptr) + static_cast<size_t>((j * N + off) * d) * esz;
+      ga.lse[ga.n] = static_cast<const float*>(cL.ptr) + j * N + off;
+      ++ga.n;
+    }
+    ga.oS[0] = H * P * N * d; ga.oS[1] = P * N * d; ga.oS[2] = d;
+    ga.lS[0] = H * P * N;     ga.lS[1] = P * N;     ga.lS[2] = 1;
+    ga.out = static_cast<float*>(gO.ptr) + off * d;
+    ga.outS[0] = H * N * d; ga.outS[1] = N * d; ga.outS[2] = d;
+    ga.out_lse = static_cast<float*>(gL.ptr) + off;
+    ga.olS[0] = H * N; ga.olS[1] = N; ga.olS[2] = 1;
+    if (launch_merge(ga, s) != cudaSuccess) return DITANGO_ERR_CUDA;
+  }
+  StepMergeArgs ma;
   std::memset(&ma, 0, sizeof(ma));
-  ma.n = static_cast<int32_t>(P);
+  ma.P = static_cast<int32_t>(P);
   ma.d = static_cast<int32_t>(d);
   ma.dtype = dtype;
-  ma.G1 = B; ma.G2 = H; ma.R = N;
-  for (int64_t j = 0; j < P; ++j) {
-    ma.O[j] = static_cast<const uint8_t*>(cO.ptr) + static_cast<size_t>(j * N * d) * elem_size(dtype);
-    ma.lse[j] = static_cast<const float*>(cL.ptr) + j * N;
+  ma.B = B; ma.H = H; ma.N = N;
+  for (int32_t i = 0; i <= P; ++i) ma.offsets[i] = static_cast<int32_t>(plan->offsets[i]);
+  for (int32_t i = 0; i < P; ++i) {
+    const uint64_t all = P == 64 ? ~uint64_t{0} : (uint64_t{1} << P) - 1;
+    const bool grp = use_group && reused[i] != 0;
+    ma.cache_set[i] = grp ? (all & ~reused[i]) : all;
+    if (grp) ma.group |= uint64_t{1} << i;
   }
-  ma.oS[0] = H * P * N * d; ma.oS[1] = P * N * d; ma.oS[2] = d;
-  ma.lS[0] = H * P * N;     ma.lS[1] = P * N;     ma.lS[2] = 1;
+  ma.cO = cO.ptr;
+  ma.cL = static_cast<const float*>(cL.ptr);
+  ma.gO = use_group ? static_cast<const float*>(gO.ptr) : nullptr;
+  ma.gL = use_group ? static_cast<const float*>(gL.ptr) : nullptr;
   ma.out = out->ptr;
   ma.outS[0] = out->stride[0]; ma.outS[1] = out->stride[2]; ma.outS[2] = out->stride[1];
   if (out_lse != nullptr) {
     ma.out_lse = static_cast<float*>(out_lse->ptr);
     ma.olS[0] = out_lse->stride[0]; ma.olS[1] = out_lse->stride[1]; ma.olS[2] = out_lse->stride[2];
   }
-  if (launch_merge(ma, s) != cudaSuccess) return DITANGO_ERR_CUDA;
+  if (launch_step_merge(ma, s) != cudaSuccess) return DITANGO_ERR_CUDA;
   if (!mark(3)) return DITANGO_ERR_CUDA;
 
+  for (uint64_t m = rebuild; m; m &= m - 1) {
+    const int32_t i = __builtin_ctzll(m);
+    plan_group_built(plan, gO.ptr, i, reused[i]);
+  }
   plan_commit(plan, reuse_mask);
   return DITANGO_OK;
 }
@@ -363,6 +419,7 @@ int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
   ma.n = sl->n;
   ma.d = static_cast<int32_t>(d);
   ma.dtype = sl->dtype;
+  ma.out_dtype = sl->dtype;
   ma.G1 = G1; ma.G2 = G2; ma.R = R;
   ma.out = out->ptr;
   for (int32_t s = 0; s < sl->n; ++s) {

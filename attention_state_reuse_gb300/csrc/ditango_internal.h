@@ -79,7 +79,8 @@ cudaError_t launch_pair_f32(int d, const PairF32Args& args, cudaStream_t stream)
 struct MergeArgs {
   int32_t n;
   int32_t d;
-  int32_t dtype;  // of the states and of out
+  int32_t dtype;      // of the states
+  int32_t out_dtype;  // of out: the states' dtype, or F32 (group states)
   int64_t G1, G2, R;
   const void* O[kMaxStates];
   const float* lse[kMaxStates];
@@ -90,6 +91,26 @@ struct MergeArgs {
   int64_t olS[3];
 };
 cudaError_t launch_merge(const MergeArgs& args, cudaStream_t stream);
+
+// The merge of one attention step: every query row r of partition i merges the cache states
+// (i, j) of the pairs in cache_set[i] and, if bit i of `group` is set, the group state of its
+// row (the composed state of partition i's reused pairs).
+struct StepMergeArgs {
+  int32_t P, d, dtype;  // dtype of the cache states and of out
+  int64_t B, H, N;
+  int32_t offsets[kMaxP + 1];
+  uint64_t cache_set[kMaxP];
+  uint64_t group;
+  const void* cO;   // [B, H, P, N, d]
+  const float* cL;  // [B, H, P, N]
+  const float* gO;  // [B, H, N, d] fp32 (may be null when group == 0)
+  const float* gL;  // [B, H, N]
+  void* out;        // element strides of b, h, r in outS (d contiguous)
+  int64_t outS[3];
+  float* out_lse;   // may be null
+  int64_t olS[3];
+};
+cudaError_t launch_step_merge(const StepMergeArgs& args, cudaStream_t stream);
 
 // 3D RoPE applied to up to two [B, N, H, d] tensors, written contiguous.
 struct RopeApplyArgs {

@@ -48,6 +48,35 @@ int plan_validate(const ditango_plan_s* p, const uint8_t* mask) {
   return DITANGO_OK;
 }
 
+uint64_t plan_reused_set(const ditango_plan_s* p, const uint8_t* mask, int32_t i) {
+  const uint8_t* m = plan_effective_mask(p, mask);
+  uint64_t set = 0;
+  for (int32_t j = 0; j < p->P; ++j)
+    if (m[i * p->P + j] == 1) set |= uint64_t{1} << j;
+  return set;
+}
+
+bool plan_group_current(const ditango_plan_s* p, const void* buf, int32_t i, uint64_t set) {
+  if (set == 0 || buf != p->group_buf || p->group_set[i] != set) return false;
+  for (int32_t j = 0; j < p->P; ++j) {
+    const size_t x = static_cast<size_t>(i) * p->P + j;
+    if (((set >> j) & 1u) && p->group_src_step[x] != p->step_computed[x]) return false;
+  }
+  return true;
+}
+
+void plan_group_built(ditango_plan_s* p, const void* buf, int32_t i, uint64_t set) {
+  if (buf != p->group_buf) {  // a new buffer holds none of the old groups
+    std::fill(p->group_set.begin(), p->group_set.end(), 0);
+    p->group_buf = buf;
+  }
+  p->group_set[i] = set;
+  for (int32_t j = 0; j < p->P; ++j) {
+    const size_t x = static_cast<size_t>(i) * p->P + j;
+    p->group_src_step[x] = p->step_computed[x];
+  }
+}
+
 void plan_commit(ditango_plan_s* p, const uint8_t* mask) {
   const uint8_t* m = plan_effective_mask(p, mask);
   for (size_t x = 0; x < p->valid.size(); ++x) {
@@ -117,6 +146,8 @@ int ditango_plan(int64_t N, int32_t P, const uint8_t* mask, ditango_plan_t* out_
   p->valid.assign(static_cast<size_t>(P) * P, 0);
   p->step_computed.assign(static_cast<size_t>(P) * P, -1);
   p->steps = 0;
+  p->group_set.assign(P, 0);
+  p->group_src_step.assign(static_cast<size_t>(P) * P, -1);
   *out_plan = p;
   return DITANGO_OK;
 }

@@ -54,11 +54,23 @@ def pair_flops(w, mask):
     return float(4.0 * w.B * w.H * w.d * (n[:, None] * n[None, :] * comp).sum())
 
 
-def merge_bytes(w):
-    """Algorithmic merge traffic: read P states (bf16 O + fp32 lse), write out + lse."""
+def merge_bytes(w, mask, group):
+    """Algorithmic traffic of a step's merge: per query row of partition i, read its cache
+    states (O in the cache dtype + fp32 lse): the computed ones, and the reused ones unless a
+    group state (fp32 O + lse) stands for them; write out and out_lse. Group states are built
+    only when the reused sets change, so the steady-state step does not count that build."""
+    import numpy as np
+
     esz = 2 if w.dtype == "bf16" else 4
-    per_row = w.P * (w.d * esz + 4) + (w.d * esz + 4)
-    return float(w.B * w.H * w.N * per_row)
+    st = w.d * esz + 4
+    mask = np.asarray(mask)
+    off = np.array([0] + list(np.cumsum([len(a) for a in np.array_split(np.arange(w.N), w.P)])))
+    total = 0
+    for i in range(w.P):
+        reused = int(mask[i].sum())
+        reads = (w.P - reused) * st + ((w.d * 4 + 4) if (group and reused) else reused * st)
+        total += int(off[i + 1] - off[i]) * (reads + st)
+    return float(w.B * w.H * total)
 
 
 def src_hash(paths):
@@ -173,10 +185,11 @@ def run_ours(args, w, rank, world):
                              start_frame=w.start_frame, device=dev)
     ws = torch.empty(max(1, dt.workspace_size(plan, B, H, d, dtype, w.rope)), dtype=torch.uint8,
                      device=dev)
+    group = dt.new_group_state(B, H, N, d, dev) if args.group else None
     anchor = np.zeros((P, P), np.uint8)
     mask = wl.step_mask(w, 1)  # the steady-state reuse step of the workload's schedule
     step = lambda m: dt.attn_step(plan, q, k, v, cO, cL, out, out_lse, reuse_mask=m, rope=rope,
-                                  softmax_scale=w.scale, workspace=ws)
+                                  softmax_scale=w.scale, workspace=ws, group=group)
 
     # anchor step (all pairs computed) fills the cache; time a few anchors for context
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -189,6 +202,13 @@ def run_ours(args, w, rank, world):
         ev[1].record()
         torch.cuda.synchronize()
         anchor_ms.append(ev[0].elapsed_time(ev[1]))
+    # the first reuse step after the anchor also builds the group states (once per change of
+    # the reused sets); it is timed on its own, the steady-state steps below reuse them
+    ev[0].record()
+    step(mask)
+    ev[1].record()
+    torch.cuda.synchronize()
+    first_reuse_ms = ev[0].elapsed_time(ev[1])
     for _ in range(args.warmup):
         step(mask)
     torch.cuda.synchronize()
@@ -259,14 +279,14 @@ def run_ours(args, w, rank, world):
     h2d = 3 * B * N * H * d * esz
     d2h = B * N * H * d * esz + B * H * N * 4
 
-    sweep = reuse_sweep(dev) if (args.sweep and world == 1) else None
+    sweep = reuse_sweep(dev, use_group=args.group) if (args.sweep and world == 1) else None
 
     flops = pair_flops(w, mask)
     peaks, peak_src = load_peaks()
     tc_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     tc_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     achieved = flops / (pair_ms * 1e-3) / 1e12
-    mbytes = merge_bytes(w)
+    mbytes = merge_bytes(w, mask, args.group)
     merge_gbs = mbytes / (merge_ms * 1e-3) / 1e9
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     ck = clocks.summary(wall0, wall1)
@@ -284,6 +304,8 @@ def run_ours(args, w, rank, world):
         "kernel_ms": {"rope": round(rope_ms, 4), "pair": round(pair_ms, 4),
                       "merge": round(merge_ms, 4)},
         "anchor_ms": round(statistics.median(anchor_ms), 4),
+        "first_reuse_step_ms": round(first_reuse_ms, 4),
+        "group_states": bool(args.group),
         "anchor_effective_tflops": round(pair_flops(w, anchor) / (statistics.median(anchor_ms) * 1e-3) / 1e12, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4),
@@ -304,7 +326,7 @@ def run_ours(args, w, rank, world):
     return line
 
 
-def reuse_sweep(dev, steps=10):
+def reuse_sweep(dev, steps=10, use_group=True):
     """Step time against the fraction of reused pairs (the reuse-fraction sweep workload).
 
     N = 32760 (21x30x52 latent), H = 40, d = 128, bf16, P in {4, 8, 16}, no RoPE, seeded
@@ -313,7 +335,8 @@ def reuse_sweep(dev, steps=10):
     mask (reuse probability 0.5, local pairs always computed). After an all-compute anchor
     step, each mask is timed over `steps` steps (CUDA events, inputs larger than L2). Reports
     ms/step, effective TFLOP/s over computed pairs, the pair kernel's time, and per P a
-    least-squares fit ms = a * computed_fraction + b with its R^2.
+    least-squares fit ms = a * computed_fraction + b with its R^2. With group states (default)
+    the untimed first step of each mask builds them and the timed steps reuse them.
     """
     import numpy as np
     import torch
@@ -334,8 +357,9 @@ def reuse_sweep(dev, steps=10):
         w = wl.get(f"sweep_P{P}")
         plan = dt.Plan(w.N, P)
         cO, cL = dt.new_state_cache(w.B, w.H, P, w.N, w.d, torch.bfloat16, dev)
+        grp = dt.new_group_state(w.B, w.H, w.N, w.d, dev) if use_group else None
         step = lambda m: dt.attn_step(plan, q, k, v, cO, cL, out, out_lse, reuse_mask=m,
-                                      softmax_scale=w.scale)
+                                      softmax_scale=w.scale, group=grp)
         masks = []
         for kind in w.schedule:
             if kind[0] == "all":
@@ -372,7 +396,7 @@ def reuse_sweep(dev, steps=10):
         result[f"P{P}"] = {"points": rows,
                            "fit": {"ms_per_computed_fraction": round(float(a), 4),
                                    "ms_at_full_reuse": round(float(b), 4), "r2": round(float(r2), 5)}}
-        del cO, cL, plan
+        del cO, cL, grp, plan
         torch.cuda.empty_cache()
     return result
 
@@ -521,6 +545,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the reuse-fraction sweep")
+    ap.add_argument("--no-group", dest="group", action="store_false",
+                    help="merge every reused state each step instead of one group state per row")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (smaller cases for profiler captures)")
     args = ap.parse_args()

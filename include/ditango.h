@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define DITANGO_ABI_VERSION 1
+#define DITANGO_ABI_VERSION 2
 #define DITANGO_MAX_PARTITIONS 64 /* P limit of a plan */
 #define DITANGO_MAX_STATES 64     /* state limit of one ditango_merge call */
 
@@ -76,10 +76,21 @@ typedef struct {
 /* The state cache of one attention layer, owned by the caller and passed unchanged every
  * step. O: [B, H, P, N, d], contiguous, dtype BF16 for bf16 inputs and F32 for f32 inputs.
  * lse: [B, H, P, N], contiguous, F32. Slot [b, h, j, r] holds the state of (partition(r), j)
- * for query row r. Contents are meaningful only for pairs this plan has computed. */
+ * for query row r. Contents are meaningful only for pairs this plan has computed.
+ * group_O, group_lse (optional: ptr NULL = not used): one composed state per query row,
+ * [B, H, N, d] and [B, H, N], contiguous, both F32 (DiTango, Methodology 2, State Composition
+ * and Dynamic Group Compose: cached states merge into a coarser group state without
+ * recomputation, and the result is itself a state). When present, a step merges every row's
+ * computed states with the single group state of its partition's reused pairs instead of with
+ * each reused state. The library builds a partition's group state (one merge of its reused
+ * cached states) at a step whose reused set differs from the one the group was built from, or
+ * when one of those pairs has been recomputed since; the plan records this, so pass the same
+ * buffers with the same plan every step (other buffers make it rebuild). */
 typedef struct {
   ditango_tensor O;
   ditango_tensor lse;
+  ditango_tensor group_O;
+  ditango_tensor group_lse;
 } ditango_state_cache;
 
 /* Precomputed 3D RoPE tables (device memory, fp32, row-major, filled by

@@ -50,7 +50,7 @@ def sample_rows(w: wl.Workload, heads_local, per_partition_random=3, seed=0):
 
 class ParityRun:
     def __init__(self, w: wl.Workload, heads=None, rows=None, device="cuda", nthreads=None,
-                 strided=False):
+                 strided=False, group=False):
         self.w = w
         self.strided = strided  # inputs and output as views into buffers with 3 spare heads
         self.device = device
@@ -62,6 +62,12 @@ class ParityRun:
         self.cO, self.cL = dt.new_state_cache(B, H, P, N, d, self.dtype, device)
         self.cO.zero_()
         self.cL.zero_()
+        # optional group states (one composed state per row over its partition's reused pairs);
+        # filled with NaN so that a group state the library failed to build shows up
+        self.group = dt.new_group_state(B, H, N, d, device) if group else None
+        if self.group is not None:
+            self.group[0].fill_(float("nan"))
+            self.group[1].fill_(float("nan"))
         self.out = self._alloc((B, N, H, d))
         self.out_lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
         self.rope = None
@@ -114,7 +120,7 @@ class ParityRun:
         before = self.gather_cache() if check else None
         dt.attn_step(self.plan, self._to_dev(q), self._to_dev(k), self._to_dev(v), self.cO,
                      self.cL, self.out, self.out_lse, reuse_mask=mask, rope=self.rope,
-                     softmax_scale=w.scale, workspace=self.ws)
+                     softmax_scale=w.scale, workspace=self.ws, group=self.group)
         torch.cuda.synchronize()
         st = dt.device_status()
         assert st == (0, 0), f"device status {st}"

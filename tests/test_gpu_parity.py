@@ -32,24 +32,53 @@ def run_all_steps(pr, steps=None):
     return errs
 
 
-def test_tiny_fp32_all_rows():
-    run_all_steps(ParityRun(wl.get("tiny_fp32")))
+@pytest.mark.parametrize("group", [False, True])
+def test_tiny_fp32_all_rows(group):
+    run_all_steps(ParityRun(wl.get("tiny_fp32"), group=group))
 
 
-def test_small_bf16_all_rows_ten_steps():
-    run_all_steps(ParityRun(wl.get("small_bf16")))
+@pytest.mark.parametrize("group", [False, True])
+def test_small_bf16_all_rows_ten_steps(group):
+    run_all_steps(ParityRun(wl.get("small_bf16"), group=group))
 
 
-def test_wan_like_reduced_rope_all_rows():
+@pytest.mark.parametrize("group", [False, True])
+def test_wan_like_reduced_rope_all_rows(group):
     # 3 frames of a 20x26 latent (N = 1560, partitions of 195 rows: two tiles, ragged),
     # start frame 5 (global time index), per-head scales, d = 128
     w = wl.scaled(wl.get("wan14b_layer"), "wan_reduced", H=4, T=3, Hl=20, Wl=26, start_frame=5)
-    run_all_steps(ParityRun(w))
+    run_all_steps(ParityRun(w, group=group))
 
 
-def test_long_720p_like_reduced_all_rows():
+@pytest.mark.parametrize("group", [False, True])
+def test_long_720p_like_reduced_all_rows(group):
     w = wl.scaled(wl.get("long_720p"), "long_reduced", H=2, T=3, Hl=15, Wl=16, steps=5)
-    run_all_steps(ParityRun(w))
+    run_all_steps(ParityRun(w, group=group))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_group_states_follow_changing_masks(dtype):
+    # the reused set of a partition changes (distance 2 -> 3 -> random -> 2), reused pairs are
+    # recomputed in between (random, all) and reused again: every change must rebuild the
+    # group state of the partitions it touches, and only a current one may be kept
+    base = wl.get("small_bf16") if dtype == "bf16" else wl.get("tiny_fp32")
+    sched = [("all",), ("dist", 2), ("dist", 2), ("dist", 3), ("random",), ("dist", 2),
+             ("dist", 2), ("all",), ("dist", 2)]
+    w = wl.Workload(f"group_{dtype}", base.index, 1, 2, base.d, base.T, base.Hl, base.Wl, 8,
+                    dtype, len(sched), 0.03, schedule=sched)
+    run_all_steps(ParityRun(w, group=True))
+
+
+def test_group_state_buffer_swap_rebuilds():
+    # a different group buffer with the same plan must not be taken for the old one
+    w = wl.scaled(wl.get("small_bf16"), "swap", H=2, steps=4)
+    pr = ParityRun(w, group=True)
+    assert pr.step(mask=np.zeros((w.P, w.P), np.uint8))["ok"]
+    assert pr.step(mask=wl.distance_mask(w.P, 2))["ok"]
+    pr.group = dt.new_group_state(w.B, w.H, w.N, w.d, "cuda")
+    pr.group[0].fill_(float("nan"))
+    pr.group[1].fill_(float("nan"))
+    assert pr.step(mask=wl.distance_mask(w.P, 2))["ok"]
 
 
 def test_rope_d64_even_table_halves():
