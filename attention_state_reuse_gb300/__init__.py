@@ -16,6 +16,7 @@ from ._build import LIB_PATH, build  # noqa: F401  (re-exported for users who bu
 __all__ = [
     "DitangoError", "Plan", "attn_step", "merge", "workspace_size", "RopeTables",
     "device_status", "new_state_cache", "new_group_state", "load_library", "SYMBOLS",
+    "planner_importance", "planner_snapshot", "planner_drift", "planner_select", "AnchorPlanner",
 ]
 
 F32, BF16 = 0, 1
@@ -31,7 +32,10 @@ STATUS = {
 SYMBOLS = [
     "ditango_plan", "ditango_plan_destroy", "ditango_plan_set_mask", "ditango_plan_check_mask",
     "ditango_plan_get_offsets", "ditango_plan_get_pairs", "ditango_plan_get_cache_state",
+    "ditango_plan_set_cache_state",
     "ditango_plan_set_profile_events", "ditango_plan_inject_fault",
+    "ditango_planner_importance", "ditango_planner_snapshot", "ditango_planner_drift",
+    "ditango_planner_select",
     "ditango_attn_step", "ditango_attn_step_static_workspace",
     "ditango_attn_step_workspace_size", "ditango_merge",
     "ditango_rope_build_tables", "ditango_device_status", "ditango_status_string",
@@ -99,8 +103,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ditango_plan_get_offsets.argtypes = [vp, P(i64)]
     lib.ditango_plan_get_pairs.argtypes = [vp, u8p, P(i32), P(i32)]
     lib.ditango_plan_get_cache_state.argtypes = [vp, u8p, P(i64), P(i64)]
+    lib.ditango_plan_set_cache_state.argtypes = [vp, u8p, P(i64), i64]
     lib.ditango_plan_set_profile_events.argtypes = [vp, P(vp)]
     lib.ditango_plan_inject_fault.argtypes = [vp, ctypes.c_int32]
+    dp = P(ctypes.c_double)
+    lib.ditango_planner_importance.argtypes = [vp, P(StateCache), vp, vp]
+    lib.ditango_planner_snapshot.argtypes = [vp, P(StateCache), P(Tensor), vp]
+    lib.ditango_planner_drift.argtypes = [vp, P(StateCache), P(Tensor), vp, vp]
+    lib.ditango_planner_select.argtypes = [vp, dp, dp, ctypes.c_double, i32, i32, u8p]
     lib.ditango_attn_step.argtypes = [vp, P(Tensor), P(Tensor), P(Tensor), P(Rope), u8p,
                                       P(StateCache), P(Tensor), P(Tensor), ctypes.c_float, vp,
                                       ctypes.c_size_t, vp]
@@ -229,6 +239,19 @@ class Plan:
             sc.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), ctypes.byref(steps)),
             "ditango_plan_get_cache_state")
         return valid.reshape(self.P, self.P), sc.reshape(self.P, self.P), steps.value
+
+    def set_cache_state(self, valid, step_computed, steps_run: int) -> None:
+        """Restores the cache bookkeeping (e.g. with a state cache restored from a checkpoint)."""
+        import numpy as np
+
+        v = np.ascontiguousarray(np.asarray(valid), dtype=np.uint8).reshape(-1)
+        sc = np.ascontiguousarray(np.asarray(step_computed), dtype=np.int64).reshape(-1)
+        if v.size != self.P * self.P or sc.size != self.P * self.P:
+            raise ValueError("valid and step_computed must hold P*P entries")
+        _check(_lib().ditango_plan_set_cache_state(
+            self._h, v.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+            sc.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(steps_run)),
+            "ditango_plan_set_cache_state")
 
     def set_mask(self, mask):
         arr, ptr = _mask_ptr(mask, self.P)
@@ -383,6 +406,95 @@ def merge(O_states, lse_states, out, out_lse=None, stream=None) -> None:
     _check(_lib().ditango_merge(ctypes.byref(sl), ctypes.byref(od),
                                 ctypes.byref(ld) if ld is not None else None, _stream_ptr(stream)),
            "ditango_merge")
+
+
+# ---------------------------------------------------------------- anchor-guided planner
+def planner_importance(plan: Plan, cache_O, cache_lse, stream=None):
+    """w [P, P] float64 (device): partition j's mean share of partition i's attention mass
+    in the cache as it stands (ditango_planner_importance; call after an anchor step)."""
+    import torch
+
+    w = torch.empty((plan.P, plan.P), dtype=torch.float64, device=cache_O.device)
+    cache = _state_cache(cache_O, cache_lse, None)
+    _check(_lib().ditango_planner_importance(plan.handle, ctypes.byref(cache),
+                                             ctypes.c_void_p(w.data_ptr()), _stream_ptr(stream)),
+           "ditango_planner_importance")
+    return w
+
+
+def planner_snapshot(plan: Plan, cache_O, cache_lse, snapshot, stream=None) -> None:
+    """Copies every partition's local states into `snapshot` [B, H, N, d] (cache dtype)."""
+    cache = _state_cache(cache_O, cache_lse, None)
+    sd = tensor_desc(snapshot)
+    _check(_lib().ditango_planner_snapshot(plan.handle, ctypes.byref(cache), ctypes.byref(sd),
+                                           _stream_ptr(stream)), "ditango_planner_snapshot")
+
+
+def planner_drift(plan: Plan, cache_O, cache_lse, snapshot, stream=None):
+    """delta [P] float64 (device): relative change of each partition's local states since
+    the snapshot."""
+    import torch
+
+    buf = torch.empty(2 * plan.P, dtype=torch.float64, device=cache_O.device)
+    cache = _state_cache(cache_O, cache_lse, None)
+    sd = tensor_desc(snapshot)
+    _check(_lib().ditango_planner_drift(plan.handle, ctypes.byref(cache), ctypes.byref(sd),
+                                        ctypes.c_void_p(buf.data_ptr()), _stream_ptr(stream)),
+           "ditango_planner_drift")
+    return buf[:plan.P]
+
+
+def planner_select(plan: Plan, w, delta, tau: float, group: int = 1, budget: int = -1):
+    """Reuse mask (numpy uint8 [P, P]) for the next step (ditango_planner_select, host)."""
+    import numpy as np
+
+    wa = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+    da = np.ascontiguousarray(np.asarray(delta, dtype=np.float64))
+    if wa.shape != (plan.P, plan.P) or da.shape != (plan.P,):
+        raise ValueError("w must be [P, P] and delta [P]")
+    mask = np.empty((plan.P, plan.P), dtype=np.uint8)
+    dp = ctypes.POINTER(ctypes.c_double)
+    _check(_lib().ditango_planner_select(plan.handle, wa.ctypes.data_as(dp), da.ctypes.data_as(dp),
+                                         float(tau), int(group), int(budget),
+                                         mask.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))),
+           "ditango_planner_select")
+    return mask
+
+
+class AnchorPlanner:
+    """Drives the reuse masks of one layer: every `anchor_every` steps an anchor step computes
+    every pair, after which the importance weights are refreshed and the local states are
+    snapshotted; on the other steps the drift since the anchor and the weights choose the mask
+    (planner_select with tau, group and budget)."""
+
+    def __init__(self, plan: Plan, cache_O, cache_lse, anchor_every: int, tau: float,
+                 group: int = 1, budget: int = -1):
+        import torch
+
+        self.plan, self.cO, self.cL = plan, cache_O, cache_lse
+        self.anchor_every, self.tau, self.group, self.budget = anchor_every, tau, group, budget
+        B, H, P, N, d = cache_O.shape
+        self.snapshot = torch.empty((B, H, N, d), dtype=cache_O.dtype, device=cache_O.device)
+        self.w = None
+        self.t = 0
+
+    def mask(self):
+        """Reuse mask for the next step."""
+        import numpy as np
+
+        if self.w is None or self.t % self.anchor_every == 0:
+            return np.zeros((self.plan.P, self.plan.P), np.uint8)
+        delta = planner_drift(self.plan, self.cO, self.cL, self.snapshot).cpu().numpy()
+        return planner_select(self.plan, self.w, delta, self.tau, self.group, self.budget)
+
+    def after_step(self, mask) -> None:
+        """Call after the step that used `mask`: an all-compute step becomes the anchor."""
+        import numpy as np
+
+        if not np.asarray(mask).any():
+            self.w = planner_importance(self.plan, self.cO, self.cL).cpu().numpy()
+            planner_snapshot(self.plan, self.cO, self.cL, self.snapshot)
+        self.t += 1
 
 
 def device_status(stream=None):

@@ -15,9 +15,12 @@ LIB_PATH = os.path.join(LIB_DIR, "libditango.so")
 OBJ_DIR = os.path.join(PKG, "_lib", "obj")
 
 SOURCES = ["api.cu", "plan.cpp", "pair_tc.cu", "pair_f32.cu", "merge.cu", "rope.cu",
-           "attn_step_static.cu"]
+           "planner.cu", "attn_step_static.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
+# host code: no FMA contraction (the planner's decisions compare sums of products, and
+# x86-64 and aarch64 builds must take the same ones)
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
+              "-ffp-contract=off", "-I" + INCLUDE, "-I" + CSRC]
 
 
 def _nvcc() -> str:

@@ -133,6 +133,46 @@ size_t rope_workspace_bytes(int64_t B, int64_t N, int64_t H, int64_t d, int32_t 
   return 2 * rope_copy_bytes(B, N, H, d, dtype);
 }
 
+
+// Validates a plan's state cache (O and lse; group states are not used here) and fills the
+// common planner arguments.
+int planner_args(ditango_plan_t plan, const ditango_state_cache* cache, PlannerArgs* a) {
+  if (plan == nullptr || cache == nullptr) return DITANGO_ERR_INVALID_ARG;
+  const ditango_tensor& cO = cache->O;
+  const ditango_tensor& cL = cache->lse;
+  if (cO.ptr == nullptr || cL.ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (cO.dtype != DITANGO_BF16 && cO.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  if (cL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  if (cO.ndim != 5 || cL.ndim != 4) return DITANGO_ERR_SHAPE;
+  const int64_t B = cO.shape[0], H = cO.shape[1], P = cO.shape[2], N = cO.shape[3], d = cO.shape[4];
+  if (P != plan->P || N != plan->N || B < 1 || H < 1 || (d != 64 && d != 128)) return DITANGO_ERR_SHAPE;
+  if (B * H > 65535) return DITANGO_ERR_SHAPE;
+  if (cL.shape[0] != B || cL.shape[1] != H || cL.shape[2] != P || cL.shape[3] != N)
+    return DITANGO_ERR_SHAPE;
+  if (!contiguous(&cO) || !contiguous(&cL)) return DITANGO_ERR_SHAPE;
+  if (!aligned16(cO.ptr) || !aligned16(cL.ptr)) return DITANGO_ERR_ALIGN;
+  std::memset(a, 0, sizeof(*a));
+  a->P = static_cast<int32_t>(P);
+  a->d = static_cast<int32_t>(d);
+  a->dtype = cO.dtype;
+  a->B = B; a->H = H; a->N = N;
+  for (int64_t i = 0; i <= P; ++i) a->offsets[i] = static_cast<int32_t>(plan->offsets[i]);
+  a->cL = static_cast<const float*>(cL.ptr);
+  a->cO = cO.ptr;
+  return DITANGO_OK;
+}
+
+// The [B, H, N, d] snapshot of the diagonal states: the cache's dtype, contiguous, aligned.
+int check_snapshot(const PlannerArgs& a, const ditango_tensor* snap) {
+  if (snap == nullptr || snap->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (snap->dtype != a.dtype) return DITANGO_ERR_DTYPE;
+  if (snap->ndim != 4 || snap->shape[0] != a.B || snap->shape[1] != a.H ||
+      snap->shape[2] != a.N || snap->shape[3] != a.d || !contiguous(snap))
+    return DITANGO_ERR_SHAPE;
+  if (!aligned16(snap->ptr)) return DITANGO_ERR_ALIGN;
+  return DITANGO_OK;
+}
+
 }  // namespace
 }  // namespace ditango
 
@@ -382,6 +422,58 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   }
   plan_commit(plan, reuse_mask);
   return DITANGO_OK;
+}
+
+// ---- anchor-guided planner ---------------------------------------------------------------
+
+int ditango_planner_importance(ditango_plan_t plan, const ditango_state_cache* cache, double* w,
+                               void* stream) {
+  PlannerArgs a;
+  int st = planner_args(plan, cache, &a);
+  if (st != DITANGO_OK) return st;
+  if (w == nullptr) return DITANGO_ERR_INVALID_ARG;
+  a.sums = w;  // summed in place, then divided by the row counts
+  a.out = w;
+  return launch_planner_importance(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DITANGO_OK
+             : DITANGO_ERR_CUDA;
+}
+
+int ditango_planner_snapshot(ditango_plan_t plan, const ditango_state_cache* cache,
+                             const ditango_tensor* snapshot, void* stream) {
+  PlannerArgs a;
+  int st = planner_args(plan, cache, &a);
+  if (st != DITANGO_OK) return st;
+  if ((st = check_snapshot(a, snapshot)) != DITANGO_OK) return st;
+  // rows of partition i in slot (i, i) of every (b, h): one 2-D copy per partition
+  const size_t esz = elem_size(a.dtype);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < a.P; ++i) {
+    const int64_t off = a.offsets[i], rows = a.offsets[i + 1] - a.offsets[i];
+    const uint8_t* src = static_cast<const uint8_t*>(a.cO) + static_cast<size_t>((i * a.N + off) * a.d) * esz;
+    uint8_t* dst = static_cast<uint8_t*>(snapshot->ptr) + static_cast<size_t>(off * a.d) * esz;
+    if (cudaMemcpy2DAsync(dst, static_cast<size_t>(a.N * a.d) * esz, src,
+                          static_cast<size_t>(a.P * a.N * a.d) * esz,
+                          static_cast<size_t>(rows * a.d) * esz, static_cast<size_t>(a.B * a.H),
+                          cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return DITANGO_ERR_CUDA;
+  }
+  return DITANGO_OK;
+}
+
+int ditango_planner_drift(ditango_plan_t plan, const ditango_state_cache* cache,
+                          const ditango_tensor* snapshot, double* delta, void* stream) {
+  PlannerArgs a;
+  int st = planner_args(plan, cache, &a);
+  if (st != DITANGO_OK) return st;
+  if ((st = check_snapshot(a, snapshot)) != DITANGO_OK) return st;
+  if (delta == nullptr) return DITANGO_ERR_INVALID_ARG;
+  a.snap = snapshot->ptr;
+  a.sums = delta;      // 2P sums first ...
+  a.out = delta;       // ... then the P drifts in the first half
+  return launch_planner_drift(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DITANGO_OK
+             : DITANGO_ERR_CUDA;
 }
 
 int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,

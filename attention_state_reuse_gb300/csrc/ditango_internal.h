@@ -112,6 +112,22 @@ struct StepMergeArgs {
 };
 cudaError_t launch_step_merge(const StepMergeArgs& args, cudaStream_t stream);
 
+// Anchor-guided planner reductions over a state cache (planner.cu). Importance accumulates
+// sums[i * P + j] over the rows of partition i and writes w = sums / rows (P*P doubles, in
+// place); drift accumulates (num_i, den_i) in sums[0..2P) and writes delta_i = sqrt(num/den).
+struct PlannerArgs {
+  int32_t P, d, dtype;  // dtype of the cache O and the snapshot
+  int64_t B, H, N;
+  int32_t offsets[kMaxP + 1];
+  const float* cL;   // cache lse [B, H, P, N]
+  const void* cO;    // cache O [B, H, P, N, d]
+  const void* snap;  // diagonal states at the anchor [B, H, N, d]
+  double* sums;      // device scratch: P*P (importance) or 2P (drift) doubles
+  double* out;       // device: w [P*P] or delta [P]
+};
+cudaError_t launch_planner_importance(const PlannerArgs& args, cudaStream_t stream);
+cudaError_t launch_planner_drift(const PlannerArgs& args, cudaStream_t stream);
+
 // 3D RoPE applied to up to two [B, N, H, d] tensors, written contiguous.
 struct RopeApplyArgs {
   int32_t n_tensors;

@@ -7,6 +7,7 @@
 // so the diagonal of a reuse mask must be 0; a pair can only be reused once a state for it
 // exists, so the first step computes every pair).
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <numeric>
@@ -191,6 +192,66 @@ int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pa
   return DITANGO_OK;
 }
 
+int ditango_planner_select(ditango_plan_t plan, const double* w, const double* delta, double tau,
+                           int32_t group, int32_t budget, uint8_t* mask) {
+  if (plan == nullptr || w == nullptr || delta == nullptr || mask == nullptr || group < 1 ||
+      !(tau >= 0.0))
+    return DITANGO_ERR_INVALID_ARG;
+  const int32_t P = plan->P;
+  for (int32_t x = 0; x < P * P; ++x)
+    if (!std::isfinite(w[x])) return DITANGO_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < P; ++i)
+    if (!std::isfinite(delta[i])) return DITANGO_ERR_INVALID_ARG;
+  struct Cand {
+    double err;
+    int32_t i, k;
+  };
+  std::vector<Cand> forced, ranked;
+  for (int32_t i = 0; i < P; ++i) {
+    for (int32_t k = 0; k * group < P; ++k) {
+      const int32_t j0 = k * group, j1 = std::min(P, j0 + group);
+      double err = 0.0;
+      bool any = false, never = false;
+      for (int32_t j = j0; j < j1; ++j) {  // ascending j: the summation order is part of the rule
+        if (j == i) continue;
+        any = true;
+        const double e = w[i * P + j] * delta[i];
+        err = err + e;
+        if (!plan->valid[static_cast<size_t>(i) * P + j]) never = true;
+      }
+      if (!any) continue;
+      (never ? forced : ranked).push_back({err, i, k});
+    }
+  }
+  std::memset(mask, 1, static_cast<size_t>(P) * P);
+  for (int32_t i = 0; i < P; ++i) mask[i * P + i] = 0;
+  int64_t computed = P;
+  auto take = [&](const Cand& c) {
+    const int32_t j0 = c.k * group, j1 = std::min(P, j0 + group);
+    for (int32_t j = j0; j < j1; ++j)
+      if (j != c.i) {
+        mask[c.i * P + j] = 0;
+        ++computed;
+      }
+  };
+  auto size_of = [&](const Cand& c) {
+    const int32_t j0 = c.k * group, j1 = std::min(P, j0 + group);
+    return (j1 - j0) - ((c.i >= j0 && c.i < j1) ? 1 : 0);
+  };
+  for (const Cand& c : forced) take(c);
+  std::stable_sort(ranked.begin(), ranked.end(), [](const Cand& a, const Cand& b) {
+    if (a.err != b.err) return a.err > b.err;
+    if (a.i != b.i) return a.i < b.i;
+    return a.k < b.k;
+  });
+  for (const Cand& c : ranked) {
+    if (!(c.err > tau)) continue;
+    if (budget >= 0 && computed + size_of(c) > budget) continue;
+    take(c);
+  }
+  return DITANGO_OK;
+}
+
 int ditango_plan_inject_fault(ditango_plan_t plan, int32_t kind) {
   if (plan == nullptr || kind < 0 || kind > 1) return DITANGO_ERR_INVALID_ARG;
   plan->inject_fault = kind;
@@ -218,6 +279,25 @@ int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* s
   if (step_computed != nullptr)
     std::copy(plan->step_computed.begin(), plan->step_computed.end(), step_computed);
   if (steps_run != nullptr) *steps_run = plan->steps;
+  return DITANGO_OK;
+}
+
+int ditango_plan_set_cache_state(ditango_plan_t plan, const uint8_t* valid,
+                                 const int64_t* step_computed, int64_t steps_run) {
+  if (plan == nullptr || valid == nullptr || step_computed == nullptr || steps_run < 0)
+    return DITANGO_ERR_INVALID_ARG;
+  const int32_t P = plan->P;
+  for (int32_t x = 0; x < P * P; ++x) {
+    if (valid[x] > 1) return DITANGO_ERR_INVALID_ARG;
+    if (valid[x] == 0 && step_computed[x] != -1) return DITANGO_ERR_INVALID_ARG;
+    if (valid[x] == 1 && (step_computed[x] < 0 || step_computed[x] >= steps_run))
+      return DITANGO_ERR_INVALID_ARG;
+    if (steps_run > 0 && x / P == x % P && valid[x] == 0) return DITANGO_ERR_INVALID_ARG;
+  }
+  std::copy(valid, valid + static_cast<size_t>(P) * P, plan->valid.begin());
+  std::copy(step_computed, step_computed + static_cast<size_t>(P) * P, plan->step_computed.begin());
+  plan->steps = steps_run;
+  std::fill(plan->group_set.begin(), plan->group_set.end(), 0);
   return DITANGO_OK;
 }
 

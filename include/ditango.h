@@ -157,12 +157,64 @@ int ditango_plan_get_pairs(ditango_plan_t plan, const uint8_t* mask, int32_t* pa
 int ditango_plan_get_cache_state(ditango_plan_t plan, uint8_t* valid, int64_t* step_computed,
                                  int64_t* steps_run);
 
+/* Restores the cache bookkeeping (the counterpart of ditango_plan_get_cache_state), for a
+ * caller that restores a saved state cache into its buffers: valid[i*P+j] in {0, 1},
+ * step_computed[i*P+j] (-1 exactly where valid is 0, else in [0, steps_run)), steps_run >= 0.
+ * The diagonal may be invalid only before the first step (steps_run = 0). Group states built
+ * under the plan are forgotten (rebuilt at their next use). Errors: INVALID_ARG (NULL
+ * pointers, values out of range); the plan is unchanged on error. */
+int ditango_plan_set_cache_state(ditango_plan_t plan, const uint8_t* valid,
+                                 const int64_t* step_computed, int64_t steps_run);
+
 /* Optional timing hook. `events` is a host array of 4 cudaEvent_t handles (created by the
  * caller, passed as void*), or NULL to switch the hook off. While set, every
  * ditango_attn_step on this plan records events[0] before the rotary prologue, events[1]
  * before the pair kernel, events[2] before the merge and events[3] after it, on the step's
  * stream, so that the caller can read per-kernel device time with cudaEventElapsedTime. */
 int ditango_plan_set_profile_events(ditango_plan_t plan, void* const* events);
+
+/* ---- anchor-guided selection planner ----------------------------------------------------
+ * Source: DiTango, Methodology 1, Anchor-Guided Selection Planner. The page names the
+ * ingredients (error as a function of partition importance w and temporal error growth delta;
+ * anchor steps that recompute everything and update w; the change of the always-computed local
+ * states as the online proxy for the drift of the remote ones; decisions per group of
+ * spatially adjacent partitions) and leaves the formulas open. These calls take the plainest
+ * reading:
+ *   w[i][j]  = mean over the rows r of partition i (and batch, heads) of exp(lse_ij - lse_i),
+ *              partition j's share of row r's attention mass (each row of w sums to 1);
+ *   delta[i] = ||O_ii(t) - O_ii(anchor)|| / ||O_ii(anchor)|| over partition i's rows;
+ *   error    = w[i][j] * delta[i], summed over a group's members j != i.
+ * cache: the layer's state cache as passed to ditango_attn_step (group states unused). */
+
+/* Importance weights from the cache as it stands (call it after an anchor step, whose every
+ * state is fresh). w: device memory for P*P doubles (row-major [i][j]); written
+ * asynchronously on `stream`. Errors: INVALID_ARG, SHAPE, DTYPE, ALIGN, CUDA. */
+int ditango_planner_importance(ditango_plan_t plan, const ditango_state_cache* cache, double* w,
+                               void* stream);
+
+/* Copies every partition's local states (cache slots (i, i) of its rows) into `snapshot`
+ * ([B, H, N, d], the cache's dtype, contiguous, 16-byte aligned; owned by the caller), to
+ * be compared against later. Call it after the anchor step. Asynchronous on `stream`. */
+int ditango_planner_snapshot(ditango_plan_t plan, const ditango_state_cache* cache,
+                             const ditango_tensor* snapshot, void* stream);
+
+/* Drift of every partition's local states since the snapshot. delta: device memory for 2*P
+ * doubles; on completion delta[0..P) holds the drifts (0 where the snapshot is all zero) and
+ * delta[P..2P) is scratch. Asynchronous on `stream`. */
+int ditango_planner_drift(ditango_plan_t plan, const ditango_state_cache* cache,
+                          const ditango_tensor* snapshot, double* delta, void* stream);
+
+/* Host only: the reuse mask (P*P bytes, 1 = reuse) for the next step from w (host, P*P) and
+ * delta (host, P). KV partitions form contiguous groups of `group` (the last may be shorter).
+ * For each query partition i and group G with a member j != i, the predicted error is the sum,
+ * in ascending j, of w[i][j] * delta[i] over those members. Groups holding a pair this plan
+ * never computed are recomputed first; the others go by decreasing error (ties: lower i, then
+ * lower G) and are recomputed when their error exceeds tau and the computed pairs, counting
+ * the P local ones, stay within `budget` (budget < 0: no limit). The local pairs are always
+ * computed. Errors: INVALID_ARG (NULL pointers, group < 1, tau < 0 or NaN, non-finite w or
+ * delta). */
+int ditango_planner_select(ditango_plan_t plan, const double* w, const double* delta, double tau,
+                           int32_t group, int32_t budget, uint8_t* mask);
 
 /* ---- fault injection (a test hook; the paper has no counterpart) ------------------------
  * kind 1 arms a one-shot fault for the next ditango_attn_step on this plan that runs the BF16
