@@ -573,24 +573,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 static_cast<size_t>(args.N) +
                             static_cast<size_t>(ui.row0 + w * kTileRows + lrow);
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.cache_O) + slot * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(o_taddr + c * 32, r);
-          uint32_t pk[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            pk[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l, __uint_as_float(r[2 * x + 1]) * inv_l);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
-          }
-        }
-        if (row_ok) args.cache_lse[slot] = (m_run + __log2f(l_run)) * kLn2;
+        // read the whole row of O in one TMEM load and hand O back to the MMA warp before the
+        // packing and the global stores, so that the next partition's first P V can start
+        uint32_t r[D];
+        if constexpr (D == 128)
+          tmem_ld_32x32b_x128(o_taddr, r);
+        else
+          tmem_ld_32x32b_x64(o_taddr, r);
         tc_fence_before_sync();
         mbar_arrive(&ctl->o_free[w]);
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            const uint32_t p0 = pack_bf16x2(__uint_as_float(r[8 * c]) * inv_l, __uint_as_float(r[8 * c + 1]) * inv_l);
+            const uint32_t p1 = pack_bf16x2(__uint_as_float(r[8 * c + 2]) * inv_l, __uint_as_float(r[8 * c + 3]) * inv_l);
+            const uint32_t p2 = pack_bf16x2(__uint_as_float(r[8 * c + 4]) * inv_l, __uint_as_float(r[8 * c + 5]) * inv_l);
+            const uint32_t p3 = pack_bf16x2(__uint_as_float(r[8 * c + 6]) * inv_l, __uint_as_float(r[8 * c + 7]) * inv_l);
+            reinterpret_cast<uint4*>(orow)[c] = make_uint4(p0, p1, p2, p3);
+          }
+          args.cache_lse[slot] = (m_run + __log2f(l_run)) * kLn2;
+        }
       }
     }
   }
