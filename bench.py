@@ -251,9 +251,9 @@ def run_ours(args, w, rank, world):
     merge_ms = statistics.mean(kev[s][2].elapsed_time(kev[s][3]) for s in range(K))
 
     # end to end through the public call with host buffers, pipelined the way a serving loop
-    # runs it: every step copies its q, k, v from pinned host memory (copy stream 1) into one of
-    # two device input sets while the step before computes, and reads its out and out_lse back
-    # into pinned host memory (copy stream 2) while the step after computes. Every step still
+    # runs it: every step copies its q, k, v from pinned host memory (one copy stream each) into
+    # one of two device input sets while the step before computes, and reads its out and
+    # out_lse back into pinned host memory (a fourth stream) while the step after computes. Every step still
     # moves its full inputs and outputs; the timed region runs from the first copy to the last
     # read-back.
     hq, hk, hv = (torch.from_numpy(a).to(dtype).pin_memory() for a in (q_np, k_np, v_np))
@@ -262,23 +262,24 @@ def run_ours(args, w, rank, world):
     inbuf = [(q, k, v), tuple(torch.empty_like(x) for x in (q, k, v))]
     outbuf = [(out, out_lse), (torch.empty_like(out), torch.empty_like(out_lse))]
     comp = torch.cuda.current_stream(dev)
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d_s = [torch.cuda.Stream(dev) for _ in range(3)]  # q, k, v copied side by side
+    d2h_s = torch.cuda.Stream(dev)
     e2e_steps = max(3, min(K, 20))
 
     def e2e_run(nsteps, start_event=None):
         done, read = [], []
         for st in range(nsteps):
             b = st % 2
-            copied = torch.cuda.Event()
-            with torch.cuda.stream(h2d_s):
-                if st == 0 and start_event is not None:
-                    h2d_s.wait_event(start_event)
-                if st >= 2:
-                    h2d_s.wait_event(done[st - 2])  # step st-2 has finished reading set b
-                for dst, src in zip(inbuf[b], (hq, hk, hv)):
+            for dst, src, cs in zip(inbuf[b], (hq, hk, hv), h2d_s):
+                copied = torch.cuda.Event()
+                with torch.cuda.stream(cs):
+                    if st == 0 and start_event is not None:
+                        cs.wait_event(start_event)
+                    if st >= 2:
+                        cs.wait_event(done[st - 2])  # step st-2 has finished reading set b
                     dst.copy_(src, non_blocking=True)
-                copied.record(h2d_s)
-            comp.wait_event(copied)
+                    copied.record(cs)
+                comp.wait_event(copied)
             if st >= 2:
                 comp.wait_event(read[st - 2])  # output set b has been read back
             qb, kb, vb = inbuf[b]
