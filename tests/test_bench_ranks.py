@@ -76,3 +76,26 @@ def test_replicas_have_own_inputs_and_same_shapes():
         assert x.shape == y.shape
         assert not np.array_equal(x, y)
     assert w.index == r0.index  # the caller's workload is left alone
+
+
+def test_algorithmic_work_accounting():
+    # hand-computed for the Wan-14B-shaped layer (B=1, H=40, d=128, N=32760, P=8, partitions of
+    # 4095 rows, |i-j| >= 2 reused: 22 computed pairs; rows of partitions 0 and 7 keep 2 computed
+    # states, the other six keep 3)
+    import bench
+    from attention_state_reuse_gb300 import workloads as wl
+
+    w = wl.get("wan14b_layer")
+    mask = wl.distance_mask(w.P, 2)
+    assert int((mask == 0).sum()) == 22
+    assert bench.pair_flops(w, mask) == 4 * 1 * 40 * 128 * 22 * 4095 * 4095
+    rows = 40 * 4095
+    state = 128 * 2 + 4
+    no_group = rows * 8 * (8 * state + state)
+    with_group = rows * (2 * (2 * state + (128 * 4 + 4) + state) + 6 * (3 * state + (128 * 4 + 4) + state))
+    assert bench.merge_bytes(w, mask, False) == no_group == 3066336000
+    assert bench.merge_bytes(w, mask, True) == with_group
+    assert abs(with_group - 1.9538e9) < 1e5
+    # all computed: no group state is read
+    zero = np.zeros((w.P, w.P), np.uint8)
+    assert bench.merge_bytes(w, zero, True) == bench.merge_bytes(w, zero, False)
