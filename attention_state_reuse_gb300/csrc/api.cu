@@ -196,12 +196,15 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
       out == nullptr)
     return DITANGO_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return DITANGO_ERR_INVALID_ARG;
-  if (q->ptr == nullptr || q->ndim != 4) return q->ptr == nullptr ? DITANGO_ERR_INVALID_ARG : DITANGO_ERR_SHAPE;
+  if (q->ndim != 4) return DITANGO_ERR_SHAPE;
   const int64_t B = q->shape[0], N = q->shape[1], H = q->shape[2], d = q->shape[3];
+  // an empty batch is refused before its (possibly NULL) pointers are looked at: the step
+  // would record every computed pair as fresh without computing one
+  if (N != plan->N || B < 1 || H < 1) return DITANGO_ERR_SHAPE;
+  if (q->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
   const int32_t dtype = q->dtype;
   const int64_t P = plan->P;
   if (dtype != DITANGO_BF16 && dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
-  if (N != plan->N || B < 1 || H < 1) return DITANGO_ERR_SHAPE;
   if (d != 64 && d != 128) return DITANGO_ERR_UNSUPPORTED;
   if (B * H * N > (int64_t{1} << 31)) return DITANGO_ERR_SHAPE;
   int st;
@@ -478,14 +481,19 @@ int ditango_planner_drift(ditango_plan_t plan, const ditango_state_cache* cache,
 
 int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
                   const ditango_tensor* out_lse, void* stream) {
-  if (sl == nullptr || out == nullptr || out->ptr == nullptr || sl->O == nullptr || sl->lse == nullptr)
+  if (sl == nullptr || out == nullptr || sl->O == nullptr || sl->lse == nullptr)
     return DITANGO_ERR_INVALID_ARG;
   if (sl->n < 1 || sl->n > kMaxStates) return DITANGO_ERR_INVALID_ARG;
   if (sl->dtype != DITANGO_BF16 && sl->dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
   const int64_t G1 = sl->shape[0], G2 = sl->shape[1], R = sl->shape[2], d = sl->shape[3];
   if (G1 < 0 || G2 < 0 || R < 0 || d < 1) return DITANGO_ERR_SHAPE;
+  if (out->ndim != 4 || out->shape[0] != G1 || out->shape[1] != G2 || out->shape[2] != R ||
+      out->shape[3] != d)
+    return DITANGO_ERR_SHAPE;
   const int64_t vec = 16 / static_cast<int64_t>(elem_size(sl->dtype));
   if (d % vec != 0) return DITANGO_ERR_SHAPE;
+  if (G1 == 0 || G2 == 0 || R == 0) return DITANGO_OK;  // no rows: nothing is read or written
+  if (out->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
   for (int a = 0; a < 3; ++a)
     if (sl->O_stride[a] % vec != 0) return DITANGO_ERR_ALIGN;
   for (int32_t s = 0; s < sl->n; ++s) {
@@ -493,9 +501,7 @@ int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
     if (!aligned16(sl->O[s])) return DITANGO_ERR_ALIGN;
   }
   if (out->dtype != sl->dtype) return DITANGO_ERR_DTYPE;
-  if (out->ndim != 4 || out->shape[0] != G1 || out->shape[1] != G2 || out->shape[2] != R ||
-      out->shape[3] != d || out->stride[3] != 1)
-    return DITANGO_ERR_SHAPE;
+  if (out->stride[3] != 1) return DITANGO_ERR_SHAPE;
   if (!aligned16(out->ptr)) return DITANGO_ERR_ALIGN;
   for (int a = 0; a < 3; ++a)
     if (out->stride[a] % vec != 0) return DITANGO_ERR_ALIGN;

@@ -233,7 +233,8 @@ int ditango_plan_inject_fault(ditango_plan_t plan, int32_t kind);
  * rotary prologue from the Causal-RoPE SP page, section 2.
  * q, k, v: [B, N, H, d] device tensors of one dtype (BF16 or F32), d contiguous; for BF16 the
  *   other strides must be multiples of 8 elements and the pointers 16-byte aligned.
- *   Supported d: 64 and 128.
+ *   Supported d: 64 and 128 (UNSUPPORTED otherwise). B and H must be at least 1: an empty
+ *   batch returns SHAPE, whatever its pointers, and leaves the plan unchanged.
  * rope: NULL = no rotation; else q and k are rotated (in fp32, rounded to the input dtype)
  *   before attention; v is never rotated.
  * reuse_mask: host P*P bytes; NULL = the plan's default mask.
@@ -286,8 +287,9 @@ size_t ditango_attn_step_workspace_size(ditango_plan_t plan, int64_t B, int64_t 
  * merge into coarser groups without recomputation; the result is itself a state).
  * Merges the n states of `states` row by row into out ([G1, G2, R, d], same dtype as the
  * states, d contiguous, strides free) and out_lse ([G1, G2, R] F32, or NULL). Reads only the
- * listed states. Errors: INVALID_ARG, SHAPE, DTYPE, ALIGN (O pointers / row strides of BF16
- * states must allow 16-byte vector access), CUDA. */
+ * listed states. With no rows (G1, G2 or R = 0) it returns DITANGO_OK without touching memory,
+ * and the data pointers may be NULL. Errors: INVALID_ARG, SHAPE, DTYPE, ALIGN (O pointers / row
+ * strides of BF16 states must allow 16-byte vector access), CUDA. */
 int ditango_merge(const ditango_state_list* states, const ditango_tensor* out,
                   const ditango_tensor* out_lse, void* stream);
 

@@ -119,6 +119,63 @@ def test_mask_checks_match_oracle_book(ditango):
     assert steps == 0 and not valid.any() and (sc == -1).all()
 
 
+def _desc(ditango, shape, dtype):
+    """A tensor descriptor with a NULL data pointer (never dereferenced by the checks below)."""
+    t = ditango.Tensor()
+    t.ptr = None
+    t.dtype = dtype
+    t.ndim = len(shape)
+    stride = 1
+    for a in reversed(range(len(shape))):
+        t.shape[a] = shape[a]
+        t.stride[a] = stride
+        stride *= max(shape[a], 1)
+    return t
+
+
+@pytest.mark.parametrize("B,H", [(0, 2), (1, 0), (0, 0)])
+def test_empty_batch_is_refused_before_any_pointer_is_read(ditango, B, H):
+    import ctypes
+
+    N, P, d = 256, 4, 64
+    plan = ditango.Plan(N, P)
+    lib = ditango.load_library()
+    q = _desc(ditango, (B, N, H, d), ditango.BF16)
+    cache = ditango.StateCache(_desc(ditango, (B, H, P, N, d), ditango.BF16),
+                               _desc(ditango, (B, H, P, N), ditango.F32))
+    out = _desc(ditango, (B, N, H, d), ditango.BF16)
+    st = lib.ditango_attn_step(plan.handle, ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                               None, None, ctypes.byref(cache), ctypes.byref(out), None,
+                               ctypes.c_float(0.125), None, ctypes.c_size_t(0), None)
+    assert ditango.STATUS[st] == "SHAPE"
+    assert plan.cache_state()[2] == 0
+
+
+@pytest.mark.parametrize("shape", [(0, 3, 5, 64), (2, 0, 5, 64), (2, 3, 0, 64)])
+def test_merge_without_rows_is_a_no_op(ditango, shape):
+    import ctypes
+
+    lib = ditango.load_library()
+    sl = ditango.StateList()
+    sl.n = 2
+    sl.dtype = ditango.BF16
+    nulls = (ctypes.c_void_p * 2)(None, None)
+    sl.O = ctypes.cast(nulls, ctypes.POINTER(ctypes.c_void_p))
+    sl.lse = ctypes.cast(nulls, ctypes.POINTER(ctypes.c_void_p))
+    for a in range(4):
+        sl.shape[a] = shape[a]
+    out = _desc(ditango, shape, ditango.BF16)
+    out_lse = _desc(ditango, shape[:3], ditango.F32)
+    st = lib.ditango_merge(ctypes.byref(sl), ctypes.byref(out), ctypes.byref(out_lse), None)
+    assert ditango.STATUS[st] == "OK"
+    # the shape of out is still checked, and a d the vector width does not divide is refused
+    bad = _desc(ditango, shape[:3] + (32,), ditango.BF16)
+    assert ditango.STATUS[lib.ditango_merge(ctypes.byref(sl), ctypes.byref(bad), None, None)] == "SHAPE"
+    sl.shape[3] = 60
+    out60 = _desc(ditango, shape[:3] + (60,), ditango.BF16)
+    assert ditango.STATUS[lib.ditango_merge(ctypes.byref(sl), ctypes.byref(out60), None, None)] == "SHAPE"
+
+
 def test_workload_mask_fractions():
     # distance-threshold masks of the configurations (fractions of reused pairs)
     assert wl.reuse_fraction(wl.distance_mask(4, 2)) == 6 / 16
