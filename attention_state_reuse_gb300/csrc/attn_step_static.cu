@@ -49,7 +49,8 @@ extern "C" int ditango_attn_step_static_workspace(
     ditango_plan_t plan, const ditango_tensor* q, const ditango_tensor* k, const ditango_tensor* v,
     const ditango_rope* rope, const uint8_t* reuse_mask, const ditango_state_cache* cache,
     const ditango_tensor* out, const ditango_tensor* out_lse, float softmax_scale, void* stream) {
-  if (plan == nullptr || q == nullptr || q->ndim != 4) return DITANGO_ERR_INVALID_ARG;
+  if (plan == nullptr || q == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (q->ndim != 4) return DITANGO_ERR_SHAPE;  // as ditango_attn_step reports it
   const size_t need = ditango_attn_step_workspace_size(plan, q->shape[0], q->shape[2],
                                                        static_cast<int32_t>(q->shape[3]), q->dtype,
                                                        rope != nullptr ? 1 : 0);

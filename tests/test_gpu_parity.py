@@ -182,6 +182,20 @@ def test_merge_grouped_equals_flat():
     assert (two_l - flat_l).abs().max().item() <= 1e-5
 
 
+def test_empty_inputs_through_the_binding():
+    # torch hands out NULL data pointers for empty CUDA tensors
+    for shape in [(2, 3, 0, 64), (0, 3, 5, 64)]:
+        O = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        L = [torch.empty(shape[:3], device="cuda") for _ in range(3)]
+        dt.merge(O, L, torch.empty_like(O[0]), torch.empty_like(L[0]))
+    plan = dt.Plan(256, 4)
+    q = torch.empty(0, 256, 2, 64, dtype=torch.bfloat16, device="cuda")
+    cO, cL = dt.new_state_cache(0, 2, 4, 256, 64, torch.bfloat16)
+    assert _status(lambda: dt.attn_step(plan, q, q, q, cO, cL, torch.empty_like(q))) == "SHAPE"
+    assert plan.cache_state()[2] == 0
+    torch.cuda.synchronize()
+
+
 # ------------------------------------------------------------------- host-detected errors
 def _small_setup(dtype=torch.bfloat16, d=64, N=256, P=4, H=2):
     q = torch.randn(1, N, H, d, device="cuda").to(dtype)
