@@ -535,7 +535,10 @@ class OracleBaseline:
                 f"extrapolated x{w.H * w.B} (RoPE) and x{w.B * w.H * w.N / self.cur_rows:.0f} (rows)")
 
 
-def run_reference(args, w):
+def run_reference(args, w, world=1):
+    """The oracle's time for the whole job's step: with `world` ranks that is `world` replicas
+    of the layer step (each rank of our arm runs one), all on the same host cores, so one
+    replica's extrapolated time is multiplied by `world`."""
     import numpy as np
 
     from attention_state_reuse_gb300 import workloads as wl
@@ -547,11 +550,14 @@ def run_reference(args, w):
         est_ms, _ = base.estimate_ms()
         if s >= args.warmup:
             vals.append(est_ms)
-    ms = statistics.median(vals)
+    ms = statistics.median(vals) * world
     mask = wl.step_mask(w, 1)
-    flops = pair_flops(w, mask)
+    flops = world * pair_flops(w, mask)
+    sample = base.sample_text()
+    if world > 1:
+        sample += f"; x{world} replicas (one per rank of the GPU arm) on the same cores"
     return {
-        "metric": METRIC, "value": round(ms, 2), "unit": "ms", "n_gpus": 1, "steps": args.steps,
+        "metric": METRIC, "value": round(ms, 2), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
@@ -559,7 +565,7 @@ def run_reference(args, w):
                    "reuse_fraction": round(float(np.asarray(mask).mean()), 4)},
         "effective_tflops": round(flops / (ms * 1e-3) / 1e12, 6),
         "cpu_baseline": {"value": round(ms, 2), "unit": "ms", "cores": base.nthreads,
-                         "kind": "oracle", "sample": base.sample_text()},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(ms, 2), "unit": "ms", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -593,7 +599,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, w)), flush=True)
+            print(json.dumps(run_reference(args, w, world)), flush=True)
         return
 
     if world > 1:

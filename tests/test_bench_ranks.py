@@ -99,3 +99,35 @@ def test_algorithmic_work_accounting():
     # all computed: no group state is read
     zero = np.zeros((w.P, w.P), np.uint8)
     assert bench.merge_bytes(w, zero, True) == bench.merge_bytes(w, zero, False)
+
+
+def test_reference_arm_counts_every_rank_replica(monkeypatch):
+    # the oracle does the whole job's work: one replica per rank of the GPU arm, same host cores
+    import argparse
+
+    import bench
+    from attention_state_reuse_gb300 import workloads as wl
+
+    class FixedOracle:
+        nthreads = 4
+
+        def __init__(self, w, budget):
+            pass
+
+        def estimate_ms(self):
+            return 1000.0, 0.1
+
+        def sample_text(self):
+            return "fixed"
+
+    monkeypatch.setattr(bench, "OracleBaseline", FixedOracle)
+    args = argparse.Namespace(steps=3, warmup=3)
+    w = wl.get("wan14b_layer")
+    one = bench.run_reference(args, w)
+    four = bench.run_reference(args, w, world=4)
+    assert one["value"] == 1000.0 and one["n_gpus"] == 1
+    assert four["value"] == 4000.0 and four["n_gpus"] == 4
+    assert four["effective_tflops"] == pytest.approx(one["effective_tflops"], rel=1e-6)
+    for line in (one, four):
+        assert line["impl"] == "reference" and line["higher_is_better"] is False
+        assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]
