@@ -126,15 +126,19 @@ def test_diagonal_only_mask_max_reuse():
 
 
 # ------------------------------------------------------------------- full sizes, sampled rows
-@pytest.mark.parametrize("name,steps,heads", [("wan14b_layer", 2, [0, 17, 39]),
-                                              ("long_720p", 2, [0, 39]),
-                                              ("sweep_P16", 2, [5, 22])])
-def test_full_size_sampled(name, steps, heads):
+@pytest.mark.parametrize("name,steps,heads,group", [("wan14b_layer", 2, [0, 17, 39], False),
+                                                    ("wan14b_layer", 3, [0, 17, 39], True),
+                                                    ("long_720p", 2, [0, 39], False),
+                                                    ("long_720p", 2, [0, 39], True),
+                                                    ("sweep_P16", 2, [5, 22], False)])
+def test_full_size_sampled(name, steps, heads, group):
+    # group=True is the configuration the benchmark times: the reuse steps merge each row's
+    # computed states with its group state (built at the first reuse step, reused after)
     w = wl.get(name)
     if name == "sweep_P16":
         w.schedule = [("all",), ("random",)]
     rows = sample_rows(w, range(len(heads)))
-    pr = ParityRun(w, heads=heads, rows=rows)
+    pr = ParityRun(w, heads=heads, rows=rows, group=group)
     run_all_steps(pr, steps)
 
 
