@@ -63,8 +63,7 @@ def _load():
         lib.oracle_round_array.argtypes = [dp, i64, i32]
         lib.oracle_rope_rotate.argtypes = [dp, dp, i32, i32, i32, i32, i64, i64, i64, dbl]
         lib.oracle_rope_apply.argtypes = [dp, dp, i64, i64, i64, i32, i32, i32, i32, i64, i64,
-                                          i64, dbl, i32, i32, i32]
-        lib.oracle_rope_rotate_f32.argtypes = [dp, dp, i32, i32, i32, i32, i64, i64, i64, dbl]
+                                          i64, dbl, i32, i32]
         lib.oracle_pair_state.argtypes = [dp, dp, dp, i64, i64, i64, i32, dbl, dp, dp, dp]
         lib.oracle_merge.argtypes = [dp, dp, i32, i32, dp, dp]
         lib.oracle_rows_step.argtypes = [dp, dp, dp, i64, i64, i64, i32, i32, i64p, u8p, dbl,
@@ -121,27 +120,17 @@ def rope_rotate(x: np.ndarray, t: int, h: int, w: int, dt: int, dh: int, dw: int
     return y
 
 
-def rope_rotate_f32(x: np.ndarray, t: int, h: int, w: int, dt: int, dh: int, dw: int,
-                    theta: float = 10000.0) -> np.ndarray:
-    """Rotate one d-vector with the rotation evaluated in fp32 (fp32 cos/sin, no FMA)."""
-    x = np.ascontiguousarray(x, dtype=np.float64)
-    y = np.empty_like(x)
-    _load().oracle_rope_rotate_f32(_dp(x), _dp(y), x.size, dt, dh, dw, t, h, w, theta)
-    return y
-
-
 def rope_apply(x: np.ndarray, Hl: int, Wl: int, start_frame: int, dt: int, dh: int, dw: int,
-               theta: float = 10000.0, round_mode: int = ROUND_NONE, f32_eval: bool = False,
+               theta: float = 10000.0, round_mode: int = ROUND_NONE,
                nthreads: int | None = None) -> np.ndarray:
-    """Rotate a [B, N, H, d] tensor by the 3D RoPE of each token's (t_global, h, w).
+    """Rotate a [B, N, H, d] tensor by the 3D RoPE of each token's (t_global, h, w), in fp64.
 
-    round_mode rounds the result to bf16 / fp32; with f32_eval the rotation is evaluated in
-    fp32 first (the precision in which a kernel takes that rounding decision)."""
+    round_mode rounds the fp64 result once (nearest-even) to bf16 / fp32."""
     x = np.ascontiguousarray(x, dtype=np.float64)
     B, N, H, d = x.shape
     y = np.empty_like(x)
     _load().oracle_rope_apply(_dp(x), _dp(y), B, N, H, d, dt, dh, dw, Hl, Wl, start_frame,
-                              theta, round_mode, int(bool(f32_eval)), nthreads or default_threads())
+                              theta, round_mode, nthreads or default_threads())
     return y
 
 
@@ -222,8 +211,9 @@ class ReuseBook:
 class OracleRun:
     """Runs the method step by step for a chosen list of query rows (b, h, r).
 
-    Each step: optional RoPE on q and k (evaluated in fp32 and rounded to the attention input
-    dtype when that dtype is bf16/fp32; in fp64 when input_round is ROUND_NONE), fresh states
+    Each step: optional RoPE on q and k (rotated in fp64, then rounded once to the attention
+    input dtype given by input_round: a bf16 pipeline hands the attention its rotated q and k
+    as bf16 tensors; ROUND_NONE keeps them in fp64), fresh states
     for the computed pairs written into the per-row cache (O rounded to the cache dtype, lse
     kept in fp32), then the merge of all P cached states of each row.
     """
@@ -248,8 +238,7 @@ class OracleRun:
     def rotate(self, x: np.ndarray) -> np.ndarray:
         r = self.rope
         return rope_apply(x, r["Hl"], r["Wl"], r.get("start_frame", 0), r["dt"], r["dh"],
-                          r["dw"], r.get("theta", 10000.0), self.input_round,
-                          self.input_round != ROUND_NONE, self.nthreads)
+                          r["dw"], r.get("theta", 10000.0), self.input_round, self.nthreads)
 
     def step(self, q: np.ndarray, k: np.ndarray, v: np.ndarray, reuse=None):
         """q, k, v: float arrays [B, N, H, d] holding the config-dtype values."""

@@ -28,7 +28,11 @@
  *   3D RoPE: token n -> (t = n / (Hl*Wl) + s, h = (n / Wl) mod Hl, w = n mod Wl);
  *     channel pair m = (2m, 2m+1); the first dt/2 pairs rotate with t, the next dh/2 with h,
  *     the last dw/2 with w; pair k of an axis of width d_a turns by pos * theta^(-2k/d_a);
- *     (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a).
+ *     (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a), in fp64; for a bf16 (fp32)
+ *     configuration the attention reads the rotated q and k stored in that dtype, i.e. the
+ *     fp64 rotation rounded once, nearest-even (a bf16 pipeline hands its attention kernel the
+ *     output of the fused projection + RoPE step as bf16 tensors: Causal-RoPE SP page,
+ *     section 2, operator fusion).
  * All arithmetic is fp64. Inputs arrive as fp64 copies of the values in the config dtype.
  */
 #include <math.h>
@@ -104,36 +108,6 @@ void oracle_rope_rotate(const double* x, double* y, int32_t d, int32_t dt, int32
   (void)dw;
 }
 
-/* Rotation evaluated the way a kernel computing in fp32 evaluates it before rounding the
- * result to bf16 (the rounding to bf16 is a quantisation step, so both sides take it from the
- * same fp32 value): cos/sin are computed in fp64 and rounded to fp32, then
- * y0 = fl32(fl32(x0 c) - fl32(x1 s)), y1 = fl32(fl32(x0 s) + fl32(x1 c)) with round-to-nearest
- * single-precision operations and no fused multiply-add (this file is built with
- * -ffp-contract=off). x holds values exactly representable in fp32. */
-void oracle_rope_rotate_f32(const double* x, double* y, int32_t d, int32_t dt, int32_t dh,
-                            int32_t dw, int64_t t, int64_t h, int64_t w, double theta) {
-  int32_t pairs = d / 2;
-  for (int32_t m = 0; m < pairs; ++m) {
-    int64_t pos;
-    int32_t k, width;
-    if (m < dt / 2) {
-      pos = t; k = m; width = dt;
-    } else if (m < dt / 2 + dh / 2) {
-      pos = h; k = m - dt / 2; width = dh;
-    } else {
-      pos = w; k = m - dt / 2 - dh / 2; width = dw;
-    }
-    double ang = (double)pos * pow(theta, -2.0 * (double)k / (double)width);
-    volatile float c = (float)cos(ang), s = (float)sin(ang);
-    volatile float x0 = (float)x[2 * m], x1 = (float)x[2 * m + 1];
-    volatile float a = x0 * c, b = x1 * s, e = x0 * s, f = x1 * c;
-    volatile float y0 = a - b, y1 = e + f;
-    y[2 * m] = (double)y0;
-    y[2 * m + 1] = (double)y1;
-  }
-  (void)dw;
-}
-
 typedef struct {
   const double* x;
   double* y;
@@ -142,7 +116,6 @@ typedef struct {
   int64_t Hl, Wl, s;
   double theta;
   int round_mode;
-  int f32_eval;
   int64_t tok_begin, tok_end; /* over B*N tokens */
 } rope_job;
 
@@ -156,28 +129,25 @@ static void* rope_worker(void* arg) {
     for (int64_t hd = 0; hd < jb->H; ++hd) {
       const double* xv = jb->x + (bn * jb->H + hd) * jb->d;
       double* yv = jb->y + (bn * jb->H + hd) * jb->d;
-      if (jb->f32_eval)
-        oracle_rope_rotate_f32(xv, yv, jb->d, jb->dt, jb->dh, jb->dw, t, h, w, jb->theta);
-      else
-        oracle_rope_rotate(xv, yv, jb->d, jb->dt, jb->dh, jb->dw, t, h, w, jb->theta);
+      oracle_rope_rotate(xv, yv, jb->d, jb->dt, jb->dh, jb->dw, t, h, w, jb->theta);
       for (int32_t e = 0; e < jb->d; ++e) yv[e] = round_to(yv[e], jb->round_mode);
     }
   }
   return NULL;
 }
 
-/* Rotate a [B, N, H, d] tensor. round_mode: 0 keep fp64, 1 round to bf16, 2 round to fp32
- * (the attention inputs are the rotated tensors in the config dtype). f32_eval: evaluate the
- * rotation in fp32 (oracle_rope_rotate_f32) before that rounding instead of in fp64. */
+/* Rotate a [B, N, H, d] tensor in fp64. round_mode: 0 keep fp64, 1 round to bf16, 2 round to
+ * fp32 (the attention inputs are the rotated tensors stored in the config dtype: one rounding of
+ * the fp64 rotation, nearest-even). */
 void oracle_rope_apply(const double* x, double* y, int64_t B, int64_t N, int64_t H, int32_t d,
                        int32_t dt, int32_t dh, int32_t dw, int64_t Hl, int64_t Wl, int64_t s,
-                       double theta, int32_t round_mode, int32_t f32_eval, int32_t nthreads) {
+                       double theta, int32_t round_mode, int32_t nthreads) {
   if (nthreads < 1) nthreads = 1;
   int64_t total = B * N;
   pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
   rope_job* jobs = (rope_job*)malloc(sizeof(rope_job) * (size_t)nthreads);
   for (int32_t i = 0; i < nthreads; ++i) {
-    rope_job jb = {x, y, B, N, H, d, dt, dh, dw, Hl, Wl, s, theta, round_mode, f32_eval,
+    rope_job jb = {x, y, B, N, H, d, dt, dh, dw, Hl, Wl, s, theta, round_mode,
                    total * i / nthreads, total * (i + 1) / nthreads};
     jobs[i] = jb;
     pthread_create(&th[i], NULL, rope_worker, &jobs[i]);

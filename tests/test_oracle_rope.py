@@ -120,16 +120,3 @@ def test_rope_apply_rounds_to_bf16_when_asked():
     y = oracle.rope_apply(x, 4, 5, 0, DT, DH, DW, round_mode=oracle.ROUND_BF16, nthreads=1)
     y64 = oracle.rope_apply(x, 4, 5, 0, DT, DH, DW, nthreads=1)
     np.testing.assert_array_equal(y, oracle.round_bf16(y64))
-
-
-def test_f32_evaluation_agrees_with_fp64_rotation():
-    # the fp32-evaluated rotation (the precision in which the bf16 rounding of the rotated
-    # inputs is decided) differs from the exact rotation only by fp32 rounding
-    rng = np.random.default_rng(6)
-    for pos in [(0, 0, 0), (3, 7, 11), (20, 29, 51), (1000, 44, 79)]:
-        x = oracle.round_array(rng.standard_normal(D) * 3, oracle.ROUND_BF16)
-        y64 = rot(x, *pos)
-        y32 = oracle.rope_rotate_f32(x, *pos, DT, DH, DW)
-        np.testing.assert_array_equal(y32, y32.astype(np.float32))  # fp32 values
-        assert np.abs(y32 - y64).max() <= 4 * 2.0 ** -24 * np.abs(x).max() * 2
-    np.testing.assert_array_equal(oracle.rope_rotate_f32(x, 0, 0, 0, DT, DH, DW), x)
