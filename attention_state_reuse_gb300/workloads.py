@@ -14,8 +14,10 @@ The latent grids stand in for Wan2.1 video latents at 480p (21x30x52) and 720p (
 
 Recipe: Q, K, V ~ N(0, 1) drawn with numpy's PCG64 generator in float32, one seed per tensor
 (config index c -> seeds 1000c+1, +2, +3); step t adds drift sigma * N(0, 1) from seed
-1000c+100+t (one generator per step, drawn in the order Q, K, V). The fp32 master values are
-rounded to the config dtype for use. Per-(tensor, head) scales U(0.5, 2) for wan14b_layer come
+1000c+100+t (tensor x = 0, 1, 2 for Q, K, V). Each tensor is drawn in consecutive chunks of
+2^22 values (flat row-major order), chunk m from its own generator seeded with [seed, m] (the
+drift: [seed, x, m]), so the values do not depend on how many threads draw them. The fp32
+master values are rounded to the config dtype for use. Per-(tensor, head) scales U(0.5, 2) for wan14b_layer come
 from seed 1000c+50. small_bf16 divides Q (and its drift) by sqrt(d) and uses softmax scale 1.
 Random masks: splitmix64 (Vigna's published generator) seeded with 1000c+7+P, one draw per
 pair in row-major order; a pair is reused iff (x >> 11) * 2^-53 < 0.5; the diagonal is always
@@ -24,6 +26,8 @@ computed (its draw is still consumed).
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -150,6 +154,32 @@ def reuse_fraction(mask: np.ndarray) -> float:
 
 
 # ---------------------------------------------------------------------------------- inputs
+CHUNK = 1 << 22
+
+
+def normal(seed, shape) -> np.ndarray:
+    """float32 N(0, 1) values of `shape`: chunk m of CHUNK consecutive values (flat order) from
+    numpy's PCG64 generator seeded with [*seed, m]; chunks are drawn on several threads."""
+    seed = list(seed) if isinstance(seed, (list, tuple)) else [seed]
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def fill(m):
+        lo, hi = m * CHUNK, min(n, (m + 1) * CHUNK)
+        np.random.default_rng(seed + [m]).standard_normal(hi - lo, dtype=np.float32,
+                                                          out=out[lo:hi])
+
+    workers = max(1, min(16, os.cpu_count() or 1, nchunks))
+    if workers == 1:
+        for m in range(nchunks):
+            fill(m)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out.reshape(shape)
+
+
 class InputStream:
     """Yields (q, k, v) as float32 numpy arrays [B, N, H, d] holding config-dtype values."""
 
@@ -160,7 +190,7 @@ class InputStream:
         c = w.index
         self.master = []
         for x in range(3):
-            a = np.random.default_rng(1000 * c + 1 + x).standard_normal(shape, dtype=np.float32)
+            a = normal(1000 * c + 1 + x, shape)
             if x == 0 and w.q_scale != 1.0:
                 a *= np.float32(w.q_scale)
             self.master.append(a)
@@ -172,9 +202,9 @@ class InputStream:
 
     def _drift(self, t):
         w = self.w
-        g = np.random.default_rng(1000 * w.index + 100 + t)
         for x in range(3):
-            dz = g.standard_normal(self.master[x].shape, dtype=np.float32) * np.float32(w.drift)
+            dz = normal([1000 * w.index + 100 + t, x], self.master[x].shape)
+            dz *= np.float32(w.drift)
             if x == 0 and w.q_scale != 1.0:
                 dz *= np.float32(w.q_scale)
             self.master[x] += dz
