@@ -126,26 +126,58 @@ def test_diagonal_only_mask_max_reuse():
 
 
 # ------------------------------------------------------------------- full sizes, sampled rows
-@pytest.mark.parametrize("name,steps,heads,group", [("wan14b_layer", 2, [0, 17, 39], False),
-                                                    ("wan14b_layer", 3, [0, 17, 39], True),
-                                                    ("long_720p", 2, [0, 39], False),
-                                                    ("long_720p", 2, [0, 39], True),
-                                                    ("sweep_P16", 2, [5, 22], False)])
-def test_full_size_sampled(name, steps, heads, group):
-    # group=True is the configuration the benchmark times: the reuse steps merge each row's
-    # computed states with its group state (built at the first reuse step, reused after)
-    w = wl.get(name)
-    if name == "sweep_P16":
-        w.schedule = [("all",), ("random",)]
-    rows = sample_rows(w, range(len(heads)))
-    pr = ParityRun(w, heads=heads, rows=rows, group=group)
+def seeded_heads(H, n_mid, seed):
+    """The first and last head plus n_mid heads drawn (seeded) from the ones between."""
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, H - 1), size=n_mid, replace=False)
+    return sorted({0, H - 1, *(int(x) for x in mid)})
+
+
+@pytest.mark.parametrize("group", [False, True])
+def test_wan14b_layer_full_schedule(group):
+    # Wan-14B-shaped layer at its stated size (N = 32760, P = 8, H = 40, RoPE, per-head
+    # scales): eight heads including the first and last, over the whole four-step schedule
+    # (anchor, then three steps reusing |i - j| >= 2; with group states the first of them builds
+    # the group states and the others reuse them, as the benchmark's steps do)
+    w = wl.get("wan14b_layer")
+    heads = seeded_heads(w.H, 6, seed=31)
+    assert len(heads) == 8
+    pr = ParityRun(w, heads=heads, rows=sample_rows(w, range(len(heads))), group=group)
+    run_all_steps(pr)
+
+
+@pytest.mark.parametrize("group,steps", [(True, 8), (False, 2)])
+def test_long_720p_full_schedule(group, steps):
+    # 720p-shaped layer at its stated size (N = 75600, P = 16, H = 40, RoPE): the first and last
+    # head and two seeded ones over the whole eight-step schedule - anchor, three steps reusing
+    # |i - j| >= 3, the refresh (all pairs) at step 4, then three reuse steps whose first
+    # rebuilds every group state from the refreshed cache
+    w = wl.get("long_720p")
+    heads = seeded_heads(w.H, 2, seed=47)
+    pr = ParityRun(w, heads=heads, rows=sample_rows(w, range(len(heads))), group=group)
     run_all_steps(pr, steps)
+
+
+@pytest.mark.parametrize("P", [4, 8, 16])
+def test_reuse_sweep_every_mask(P):
+    # the reuse-fraction sweep at its stated size (N = 32760, H = 40, d = 128, no RoPE) in the
+    # order the benchmark times it: all pairs computed, every distance threshold from P - 1 down
+    # to the smallest (87.5% / 87.5% / 82.0% reused at P = 4 / 8 / 16), then the seeded random
+    # mask; group states on, two heads
+    w = wl.get(f"sweep_P{P}")
+    heads = seeded_heads(w.H, 0, seed=0)
+    pr = ParityRun(w, heads=heads, rows=sample_rows(w, range(len(heads))), group=True)
+    errs = run_all_steps(pr)
+    assert len(errs) == len(w.schedule) == P + 1 - {4: 1, 8: 1, 16: 2}[P] + 1
 
 
 # ------------------------------------------------------------------- merge entry point
 @pytest.mark.parametrize("dtype,n,d", [(torch.bfloat16, 1, 128), (torch.bfloat16, 7, 64),
                                        (torch.bfloat16, 64, 128), (torch.float32, 5, 64),
-                                       (torch.float32, 16, 128)])
+                                       (torch.float32, 16, 128),
+                                       # head dims whose vectors per row are no power of two
+                                       (torch.bfloat16, 3, 96), (torch.bfloat16, 9, 40),
+                                       (torch.float32, 4, 24), (torch.float32, 11, 12)])
 def test_merge_entry_point(dtype, n, d):
     import oracle
 
