@@ -17,6 +17,7 @@ __all__ = [
     "DitangoError", "Plan", "attn_step", "merge", "workspace_size", "RopeTables",
     "device_status", "new_state_cache", "new_group_state", "load_library", "SYMBOLS",
     "planner_importance", "planner_snapshot", "planner_drift", "planner_select", "AnchorPlanner",
+    "new_host_states", "cache_slot_map",
 ]
 
 F32, BF16 = 0, 1
@@ -39,7 +40,7 @@ SYMBOLS = [
     "ditango_attn_step", "ditango_attn_step_static_workspace",
     "ditango_attn_step_workspace_size", "ditango_merge",
     "ditango_rope_build_tables", "ditango_device_status", "ditango_status_string",
-    "ditango_version",
+    "ditango_version", "ditango_cache_slot_map",
 ]
 
 
@@ -56,14 +57,18 @@ class Tensor(ctypes.Structure):
 
 
 class StateCache(ctypes.Structure):
-    _fields_ = [("O", Tensor), ("lse", Tensor), ("group_O", Tensor), ("group_lse", Tensor)]
+    _fields_ = [("O", Tensor), ("lse", Tensor), ("group_O", Tensor), ("group_lse", Tensor),
+                ("host_O", Tensor), ("host_lse", Tensor)]
 
 
-def _state_cache(cache_O, cache_lse, group):
+def _state_cache(cache_O, cache_lse, group, host=None):
     c = StateCache(tensor_desc(cache_O), tensor_desc(cache_lse))
     if group is not None:
         c.group_O = tensor_desc(group[0])
         c.group_lse = tensor_desc(group[1])
+    if host is not None:
+        c.host_O = host_tensor_desc(host[0])
+        c.host_lse = host_tensor_desc(host[1])
     return c
 
 
@@ -73,7 +78,10 @@ class Rope(ctypes.Structure):
                 ("cos_w", ctypes.c_void_p), ("sin_w", ctypes.c_void_p),
                 ("T_tab", ctypes.c_int64), ("Hl", ctypes.c_int64), ("Wl", ctypes.c_int64),
                 ("dt", ctypes.c_int32), ("dh", ctypes.c_int32), ("dw", ctypes.c_int32),
-                ("start_frame", ctypes.c_int64)]
+                ("start_frame", ctypes.c_int64),
+                ("cos_t_lo", ctypes.c_void_p), ("sin_t_lo", ctypes.c_void_p),
+                ("cos_h_lo", ctypes.c_void_p), ("sin_h_lo", ctypes.c_void_p),
+                ("cos_w_lo", ctypes.c_void_p), ("sin_w_lo", ctypes.c_void_p)]
 
 
 class StateList(ctypes.Structure):
@@ -125,6 +133,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ditango_status_string.argtypes = [ctypes.c_int]
     lib.ditango_status_string.restype = ctypes.c_char_p
     lib.ditango_version.argtypes = []
+    lib.ditango_cache_slot_map.argtypes = [i32, i32, P(ctypes.c_int8)]
     return lib
 
 
@@ -167,6 +176,20 @@ def tensor_desc(t) -> Tensor:
     """ditango_tensor describing a CUDA torch tensor (no copy)."""
     if not t.is_cuda:
         raise ValueError("tensors passed to the library must live on a CUDA device")
+    d = Tensor()
+    d.ptr = t.data_ptr()
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for a in range(t.dim()):
+        d.shape[a] = t.shape[a]
+        d.stride[a] = t.stride(a)
+    return d
+
+
+def host_tensor_desc(t) -> Tensor:
+    """ditango_tensor describing a page-locked (pinned) CPU torch tensor (no copy)."""
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("host storage must be a pinned CPU tensor")
     d = Tensor()
     d.ptr = t.data_ptr()
     d.dtype = _dtype_code(t)
@@ -284,6 +307,29 @@ def new_state_cache(B, H, P, N, d, dtype, device="cuda"):
     return O, lse
 
 
+def new_host_states(B, H, P, N, d, dtype):
+    """Allocates host storage for a state cache whose device part keeps S < P slots per row:
+    O [B, H, P, N, d] and lse [B, H, P, N] fp32 in page-locked host memory. Pass them as
+    `host=` to attn_step (and the planner calls) together with a device cache made by
+    new_state_cache(B, H, S, N, d, ...)."""
+    import torch
+
+    O = torch.empty((B, H, P, N, d), dtype=dtype, pin_memory=True)
+    lse = torch.empty((B, H, P, N), dtype=torch.float32, pin_memory=True)
+    return O, lse
+
+
+def cache_slot_map(P: int, S: int):
+    """[P, P] int8 numpy array: the device slot of pair (i, j) when the device cache keeps S
+    of the P states per row, -1 for a pair kept in host storage (ditango_cache_slot_map)."""
+    import numpy as np
+
+    out = np.empty(P * P, dtype=np.int8)
+    _check(_lib().ditango_cache_slot_map(int(P), int(S), out.ctypes.data_as(
+        ctypes.POINTER(ctypes.c_int8))), "ditango_cache_slot_map")
+    return out.reshape(P, P)
+
+
 def new_group_state(B, H, N, d, device="cuda"):
     """Allocates the optional group states of a cache: O [B, H, N, d] and lse [B, H, N], fp32.
     Pass them as `group=` to attn_step with the same plan every step."""
@@ -318,6 +364,10 @@ class RopeTables:
         self.sin_h = torch.empty_like(self.cos_h)
         self.cos_w = torch.empty((self.Wl, self.dw // 2), **f)
         self.sin_w = torch.empty_like(self.cos_w)
+        # residuals: table + residual carries cos and sin to about 48 bits
+        self.cos_t_lo, self.sin_t_lo = torch.empty_like(self.cos_t), torch.empty_like(self.cos_t)
+        self.cos_h_lo, self.sin_h_lo = torch.empty_like(self.cos_h), torch.empty_like(self.cos_h)
+        self.cos_w_lo, self.sin_w_lo = torch.empty_like(self.cos_w), torch.empty_like(self.cos_w)
         s = self.struct()
         _check(_lib().ditango_rope_build_tables(ctypes.byref(s), float(theta), _stream_ptr(stream)),
                "ditango_rope_build_tables")
@@ -330,18 +380,22 @@ class RopeTables:
         r.T_tab, r.Hl, r.Wl = self.T_tab, self.Hl, self.Wl
         r.dt, r.dh, r.dw = self.dt, self.dh, self.dw
         r.start_frame = self.start_frame
+        r.cos_t_lo, r.sin_t_lo = self.cos_t_lo.data_ptr(), self.sin_t_lo.data_ptr()
+        r.cos_h_lo, r.sin_h_lo = self.cos_h_lo.data_ptr(), self.sin_h_lo.data_ptr()
+        r.cos_w_lo, r.sin_w_lo = self.cos_w_lo.data_ptr(), self.sin_w_lo.data_ptr()
         return r
 
 
 def attn_step(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None, reuse_mask=None,
               rope: RopeTables | None = None, softmax_scale: float | None = None, workspace=None,
-              stream=None, group=None) -> None:
+              stream=None, group=None, host=None) -> None:
     """One attention-layer step (ditango_attn_step), asynchronous on `stream`. `group`: the
-    cache's optional group states (new_group_state), or None."""
+    cache's optional group states (new_group_state), or None. `host`: the cache's optional host
+    storage (new_host_states) when cache_O keeps fewer than P slots per row, or None."""
     if softmax_scale is None:
         softmax_scale = q.shape[-1] ** -0.5
     qd, kd, vd, od = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
-    cache = _state_cache(cache_O, cache_lse, group)
+    cache = _state_cache(cache_O, cache_lse, group, host)
     ld = tensor_desc(out_lse) if out_lse is not None else None
     rs = rope.struct() if rope is not None else None
     arr, mptr = _mask_ptr(reuse_mask, plan.P)
@@ -358,14 +412,14 @@ def attn_step(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None, reuse_
 def attn_step_static_workspace(plan: Plan, q, k, v, cache_O, cache_lse, out, out_lse=None,
                                reuse_mask=None, rope: RopeTables | None = None,
                                softmax_scale: float | None = None, stream=None,
-                               group=None) -> None:
+                               group=None, host=None) -> None:
     """ditango_attn_step_static_workspace: the step without a caller workspace, for callers
     that cannot allocate device memory; its scratch lives in a 64 MiB array inside the
     library (steps needing more are refused with WORKSPACE). Concurrent calls race on it."""
     if softmax_scale is None:
         softmax_scale = q.shape[-1] ** -0.5
     qd, kd, vd, od = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
-    cache = _state_cache(cache_O, cache_lse, group)
+    cache = _state_cache(cache_O, cache_lse, group, host)
     ld = tensor_desc(out_lse) if out_lse is not None else None
     rs = rope.struct() if rope is not None else None
     arr, mptr = _mask_ptr(reuse_mask, plan.P)
@@ -409,34 +463,34 @@ def merge(O_states, lse_states, out, out_lse=None, stream=None) -> None:
 
 
 # ---------------------------------------------------------------- anchor-guided planner
-def planner_importance(plan: Plan, cache_O, cache_lse, stream=None):
+def planner_importance(plan: Plan, cache_O, cache_lse, stream=None, host=None):
     """w [P, P] float64 (device): partition j's mean share of partition i's attention mass
     in the cache as it stands (ditango_planner_importance; call after an anchor step)."""
     import torch
 
     w = torch.empty((plan.P, plan.P), dtype=torch.float64, device=cache_O.device)
-    cache = _state_cache(cache_O, cache_lse, None)
+    cache = _state_cache(cache_O, cache_lse, None, host)
     _check(_lib().ditango_planner_importance(plan.handle, ctypes.byref(cache),
                                              ctypes.c_void_p(w.data_ptr()), _stream_ptr(stream)),
            "ditango_planner_importance")
     return w
 
 
-def planner_snapshot(plan: Plan, cache_O, cache_lse, snapshot, stream=None) -> None:
+def planner_snapshot(plan: Plan, cache_O, cache_lse, snapshot, stream=None, host=None) -> None:
     """Copies every partition's local states into `snapshot` [B, H, N, d] (cache dtype)."""
-    cache = _state_cache(cache_O, cache_lse, None)
+    cache = _state_cache(cache_O, cache_lse, None, host)
     sd = tensor_desc(snapshot)
     _check(_lib().ditango_planner_snapshot(plan.handle, ctypes.byref(cache), ctypes.byref(sd),
                                            _stream_ptr(stream)), "ditango_planner_snapshot")
 
 
-def planner_drift(plan: Plan, cache_O, cache_lse, snapshot, stream=None):
+def planner_drift(plan: Plan, cache_O, cache_lse, snapshot, stream=None, host=None):
     """delta [P] float64 (device): relative change of each partition's local states since
     the snapshot."""
     import torch
 
     buf = torch.empty(2 * plan.P, dtype=torch.float64, device=cache_O.device)
-    cache = _state_cache(cache_O, cache_lse, None)
+    cache = _state_cache(cache_O, cache_lse, None, host)
     sd = tensor_desc(snapshot)
     _check(_lib().ditango_planner_drift(plan.handle, ctypes.byref(cache), ctypes.byref(sd),
                                         ctypes.c_void_p(buf.data_ptr()), _stream_ptr(stream)),

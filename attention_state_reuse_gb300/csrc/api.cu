@@ -82,6 +82,14 @@ int check_bnhd(const ditango_tensor* t, int64_t B, int64_t N, int64_t H, int64_t
   return DITANGO_OK;
 }
 
+// Every stride of the first `n` dims at least 1 (no aliasing of distinct elements through a
+// zero stride, no negative offsets).
+bool positive_strides(const ditango_tensor* t, int n) {
+  for (int a = 0; a < n; ++a)
+    if (t->stride[a] < 1) return false;
+  return true;
+}
+
 bool contiguous(const ditango_tensor* t) {
   int64_t s = 1;
   for (int a = t->ndim - 1; a >= 0; --a) {
@@ -114,8 +122,9 @@ int check_rope(const ditango_rope* r, int64_t N, int64_t d) {
   if (r->Hl < 1 || r->Wl < 1 || r->T_tab < 1 || r->start_frame < 0) return DITANGO_ERR_INVALID_ARG;
   if (N % (r->Hl * r->Wl) != 0) return DITANGO_ERR_SHAPE;
   if (r->start_frame + N / (r->Hl * r->Wl) > r->T_tab) return DITANGO_ERR_SHAPE;
-  if ((r->dt && (!r->cos_t || !r->sin_t)) || (r->dh && (!r->cos_h || !r->sin_h)) ||
-      (r->dw && (!r->cos_w || !r->sin_w)))
+  if ((r->dt && (!r->cos_t || !r->sin_t || !r->cos_t_lo || !r->sin_t_lo)) ||
+      (r->dh && (!r->cos_h || !r->sin_h || !r->cos_h_lo || !r->sin_h_lo)) ||
+      (r->dw && (!r->cos_w || !r->sin_w || !r->cos_w_lo || !r->sin_w_lo)))
     return DITANGO_ERR_INVALID_ARG;
   return DITANGO_OK;
 }
@@ -134,31 +143,82 @@ size_t rope_workspace_bytes(int64_t B, int64_t N, int64_t H, int64_t d, int32_t 
 }
 
 
-// Validates a plan's state cache (O and lse; group states are not used here) and fills the
-// common planner arguments.
-int planner_args(ditango_plan_t plan, const ditango_state_cache* cache, PlannerArgs* a) {
-  if (plan == nullptr || cache == nullptr) return DITANGO_ERR_INVALID_ARG;
+// Validates the state cache's O and lse (device, [B, H, S, N, d] and [B, H, S, N]) and its
+// optional host storage ([B, H, P, N, d] and [B, H, P, N], page-locked host memory the device
+// can address), and fills `loc` with the pointers and the slot map. S = P without host storage.
+int cache_loc(const ditango_state_cache* cache, int64_t B, int64_t H, int64_t P, int64_t N,
+              int64_t d, int32_t dtype, CacheLoc* loc) {
   const ditango_tensor& cO = cache->O;
   const ditango_tensor& cL = cache->lse;
   if (cO.ptr == nullptr || cL.ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
-  if (cO.dtype != DITANGO_BF16 && cO.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
-  if (cL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  if (cO.dtype != dtype || cL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
   if (cO.ndim != 5 || cL.ndim != 4) return DITANGO_ERR_SHAPE;
-  const int64_t B = cO.shape[0], H = cO.shape[1], P = cO.shape[2], N = cO.shape[3], d = cO.shape[4];
-  if (P != plan->P || N != plan->N || B < 1 || H < 1 || (d != 64 && d != 128)) return DITANGO_ERR_SHAPE;
-  if (B * H > 65535) return DITANGO_ERR_SHAPE;
-  if (cL.shape[0] != B || cL.shape[1] != H || cL.shape[2] != P || cL.shape[3] != N)
+  const int64_t S = cO.shape[2];
+  const bool host = cache->host_O.ptr != nullptr || cache->host_lse.ptr != nullptr;
+  if (S < 1 || S > P || (!host && S != P)) return DITANGO_ERR_SHAPE;
+  if (cO.shape[0] != B || cO.shape[1] != H || cO.shape[3] != N || cO.shape[4] != d ||
+      !contiguous(&cO))
     return DITANGO_ERR_SHAPE;
-  if (!contiguous(&cO) || !contiguous(&cL)) return DITANGO_ERR_SHAPE;
+  if (cL.shape[0] != B || cL.shape[1] != H || cL.shape[2] != S || cL.shape[3] != N ||
+      !contiguous(&cL))
+    return DITANGO_ERR_SHAPE;
   if (!aligned16(cO.ptr) || !aligned16(cL.ptr)) return DITANGO_ERR_ALIGN;
+  std::memset(loc, 0, sizeof(*loc));
+  loc->dO = cO.ptr;
+  loc->dL = static_cast<float*>(cL.ptr);
+  loc->S = static_cast<int32_t>(S);
+  if (host) {
+    const ditango_tensor& hO = cache->host_O;
+    const ditango_tensor& hL = cache->host_lse;
+    if (hO.ptr == nullptr || hL.ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+    if (hO.dtype != dtype || hL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+    if (hO.ndim != 5 || hO.shape[0] != B || hO.shape[1] != H || hO.shape[2] != P ||
+        hO.shape[3] != N || hO.shape[4] != d || !contiguous(&hO))
+      return DITANGO_ERR_SHAPE;
+    if (hL.ndim != 4 || hL.shape[0] != B || hL.shape[1] != H || hL.shape[2] != P ||
+        hL.shape[3] != N || !contiguous(&hL))
+      return DITANGO_ERR_SHAPE;
+    if (!aligned16(hO.ptr) || !aligned16(hL.ptr)) return DITANGO_ERR_ALIGN;
+    // the device addresses of page-locked host memory (the same pointers under unified
+    // addressing); anything else the kernels could not reach
+    void* dev_ptr[2] = {nullptr, nullptr};
+    const void* host_ptr[2] = {hO.ptr, hL.ptr};
+    for (int x = 0; x < 2; ++x) {
+      cudaPointerAttributes attr;
+      if (cudaPointerGetAttributes(&attr, host_ptr[x]) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DITANGO_ERR_INVALID_ARG;
+      }
+      if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+        return DITANGO_ERR_INVALID_ARG;
+      dev_ptr[x] = attr.devicePointer;
+    }
+    loc->hO = dev_ptr[0];
+    loc->hL = static_cast<float*>(dev_ptr[1]);
+  }
+  cache_slot_map(static_cast<int32_t>(P), static_cast<int32_t>(S), loc->slot);
+  return DITANGO_OK;
+}
+
+// Validates a plan's state cache (O and lse, and host storage if any; group states are not used
+// here) and fills the common planner arguments.
+int planner_args(ditango_plan_t plan, const ditango_state_cache* cache, PlannerArgs* a) {
+  if (plan == nullptr || cache == nullptr) return DITANGO_ERR_INVALID_ARG;
+  const ditango_tensor& cO = cache->O;
+  if (cO.ptr == nullptr || cache->lse.ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
+  if (cO.dtype != DITANGO_BF16 && cO.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
+  if (cO.ndim != 5) return DITANGO_ERR_SHAPE;
+  const int64_t B = cO.shape[0], H = cO.shape[1], P = plan->P, N = cO.shape[3], d = cO.shape[4];
+  if (N != plan->N || B < 1 || H < 1 || (d != 64 && d != 128)) return DITANGO_ERR_SHAPE;
+  if (B * H > 65535) return DITANGO_ERR_SHAPE;
   std::memset(a, 0, sizeof(*a));
+  const int st = cache_loc(cache, B, H, P, N, d, cO.dtype, &a->cache);
+  if (st != DITANGO_OK) return st;
   a->P = static_cast<int32_t>(P);
   a->d = static_cast<int32_t>(d);
   a->dtype = cO.dtype;
   a->B = B; a->H = H; a->N = N;
   for (int64_t i = 0; i <= P; ++i) a->offsets[i] = static_cast<int32_t>(plan->offsets[i]);
-  a->cL = static_cast<const float*>(cL.ptr);
-  a->cO = cO.ptr;
   return DITANGO_OK;
 }
 
@@ -218,18 +278,10 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     if (out_lse->ndim != 3 || out_lse->shape[0] != B || out_lse->shape[1] != H ||
         out_lse->shape[2] != N)
       return DITANGO_ERR_SHAPE;
+    if (!positive_strides(out_lse, 3)) return DITANGO_ERR_SHAPE;
   }
-  const ditango_tensor& cO = cache->O;
-  const ditango_tensor& cL = cache->lse;
-  if (cO.ptr == nullptr || cL.ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
-  if (cO.dtype != dtype || cL.dtype != DITANGO_F32) return DITANGO_ERR_DTYPE;
-  if (cO.ndim != 5 || cO.shape[0] != B || cO.shape[1] != H || cO.shape[2] != P ||
-      cO.shape[3] != N || cO.shape[4] != d || !contiguous(&cO))
-    return DITANGO_ERR_SHAPE;
-  if (cL.ndim != 4 || cL.shape[0] != B || cL.shape[1] != H || cL.shape[2] != P ||
-      cL.shape[3] != N || !contiguous(&cL))
-    return DITANGO_ERR_SHAPE;
-  if (!aligned16(cO.ptr) || !aligned16(cL.ptr)) return DITANGO_ERR_ALIGN;
+  // the cache's pointers are checked here; whether host storage can be reached is asked of
+  // the CUDA runtime only after the other arguments passed
   const ditango_tensor& gO = cache->group_O;
   const ditango_tensor& gL = cache->group_lse;
   const bool use_group = gO.ptr != nullptr;
@@ -252,6 +304,8 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   }
   if ((st = plan_validate(plan, reuse_mask)) != DITANGO_OK) return st;
   const uint8_t* mask = plan_effective_mask(plan, reuse_mask);
+  CacheLoc loc;
+  if ((st = cache_loc(cache, B, H, P, N, d, dtype, &loc)) != DITANGO_OK) return st;
 
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != DITANGO_OK) return st;
@@ -276,6 +330,9 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     rq.cos_t = rope->cos_t; rq.sin_t = rope->sin_t;
     rq.cos_h = rope->cos_h; rq.sin_h = rope->sin_h;
     rq.cos_w = rope->cos_w; rq.sin_w = rope->sin_w;
+    rq.cos_t_lo = rope->cos_t_lo; rq.sin_t_lo = rope->sin_t_lo;
+    rq.cos_h_lo = rope->cos_h_lo; rq.sin_h_lo = rope->sin_h_lo;
+    rq.cos_w_lo = rope->cos_w_lo; rq.sin_w_lo = rope->sin_w_lo;
     rq.Hl = static_cast<int32_t>(rope->Hl);
     rq.Wl = static_cast<int32_t>(rope->Wl);
     rq.start_frame = static_cast<int32_t>(rope->start_frame);
@@ -304,6 +361,9 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     ra.cos_t = rope->cos_t; ra.sin_t = rope->sin_t;
     ra.cos_h = rope->cos_h; ra.sin_h = rope->sin_h;
     ra.cos_w = rope->cos_w; ra.sin_w = rope->sin_w;
+    ra.cos_t_lo = rope->cos_t_lo; ra.sin_t_lo = rope->sin_t_lo;
+    ra.cos_h_lo = rope->cos_h_lo; ra.sin_h_lo = rope->sin_h_lo;
+    ra.cos_w_lo = rope->cos_w_lo; ra.sin_w_lo = rope->sin_w_lo;
     ra.Hl = rope->Hl; ra.Wl = rope->Wl; ra.start_frame = rope->start_frame;
     ra.dt = rope->dt; ra.dh = rope->dh; ra.dw = rope->dw;
     if (launch_rope_apply(ra, s) != cudaSuccess) return DITANGO_ERR_CUDA;
@@ -332,8 +392,7 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     PairTcArgs pa;
     pa.sched = sched;
     pa.N = N;
-    pa.cache_O = cO.ptr;
-    pa.cache_lse = static_cast<float*>(cL.ptr);
+    pa.cache = loc;
     pa.scale_log2 = softmax_scale * 1.4426950408889634f;
     pa.err = dev->err_ptr;
     pa.rope = rq;
@@ -353,46 +412,22 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
       pa.ks[a] = ks[a];
       pa.vs[a] = v->stride[a];
     }
-    pa.cache_O = static_cast<float*>(cO.ptr);
-    pa.cache_lse = static_cast<float*>(cL.ptr);
+    pa.cache = loc;
     pa.scale = softmax_scale;
     if (launch_pair_f32(static_cast<int>(d), pa, s) != cudaSuccess) return DITANGO_ERR_CUDA;
   }
 
   // ---- 3. merge: each row's computed states with its reused ones, or with the group state of
-  // its partition's reused pairs (built first where it is missing or out of date)
+  // its partition's reused pairs (built in the same pass where it is missing or out of date)
   if (!mark(2)) return DITANGO_ERR_CUDA;
-  const size_t esz = elem_size(dtype);
   uint64_t reused[kMaxP] = {}, rebuild = 0;
   for (int32_t i = 0; i < P; ++i) {
     reused[i] = plan_reused_set(plan, reuse_mask, i);
     if (use_group && reused[i] != 0 && !plan_group_current(plan, gO.ptr, i, reused[i]))
       rebuild |= uint64_t{1} << i;
   }
-  for (uint64_t m = rebuild; m; m &= m - 1) {
-    const int32_t i = __builtin_ctzll(m);
-    plan->group_set[i] = 0;  // invalid until this build has been launched
-    const int64_t off = plan->offsets[i];
-    MergeArgs ga;
-    std::memset(&ga, 0, sizeof(ga));
-    ga.d = static_cast<int32_t>(d);
-    ga.dtype = dtype;
-    ga.out_dtype = DITANGO_F32;
-    ga.G1 = B; ga.G2 = H; ga.R = plan->offsets[i + 1] - off;
-    for (uint64_t r = reused[i]; r; r &= r - 1) {
-      const int32_t j = __builtin_ctzll(r);
-      ga.O[ga.n] = static_cast<const uint8_t*>(cO.ptr) + static_cast<size_t>((j * N + off) * d) * esz;
-      ga.lse[ga.n] = static_cast<const float*>(cL.ptr) + j * N + off;
-      ++ga.n;
-    }
-    ga.oS[0] = H * P * N * d; ga.oS[1] = P * N * d; ga.oS[2] = d;
-    ga.lS[0] = H * P * N;     ga.lS[1] = P * N;     ga.lS[2] = 1;
-    ga.out = static_cast<float*>(gO.ptr) + off * d;
-    ga.outS[0] = H * N * d; ga.outS[1] = N * d; ga.outS[2] = d;
-    ga.out_lse = static_cast<float*>(gL.ptr) + off;
-    ga.olS[0] = H * N; ga.olS[1] = N; ga.olS[2] = 1;
-    if (launch_merge(ga, s) != cudaSuccess) return DITANGO_ERR_CUDA;
-  }
+  for (uint64_t m = rebuild; m; m &= m - 1)
+    plan->group_set[__builtin_ctzll(m)] = 0;  // invalid until this build has been launched
   StepMergeArgs ma;
   std::memset(&ma, 0, sizeof(ma));
   ma.P = static_cast<int32_t>(P);
@@ -404,12 +439,13 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     const uint64_t all = P == 64 ? ~uint64_t{0} : (uint64_t{1} << P) - 1;
     const bool grp = use_group && reused[i] != 0;
     ma.cache_set[i] = grp ? (all & ~reused[i]) : all;
+    ma.reused_set[i] = reused[i];
     if (grp) ma.group |= uint64_t{1} << i;
   }
-  ma.cO = cO.ptr;
-  ma.cL = static_cast<const float*>(cL.ptr);
-  ma.gO = use_group ? static_cast<const float*>(gO.ptr) : nullptr;
-  ma.gL = use_group ? static_cast<const float*>(gL.ptr) : nullptr;
+  ma.rebuild = rebuild;
+  ma.cache = loc;
+  ma.gO = use_group ? static_cast<float*>(gO.ptr) : nullptr;
+  ma.gL = use_group ? static_cast<float*>(gL.ptr) : nullptr;
   ma.out = out->ptr;
   ma.outS[0] = out->stride[0]; ma.outS[1] = out->stride[2]; ma.outS[2] = out->stride[1];
   if (out_lse != nullptr) {
@@ -448,15 +484,19 @@ int ditango_planner_snapshot(ditango_plan_t plan, const ditango_state_cache* cac
   int st = planner_args(plan, cache, &a);
   if (st != DITANGO_OK) return st;
   if ((st = check_snapshot(a, snapshot)) != DITANGO_OK) return st;
-  // rows of partition i in slot (i, i) of every (b, h): one 2-D copy per partition
+  // rows of partition i in the device slot of (i, i) of every (b, h) (the local pair is always
+  // on the device): one 2-D copy per partition
   const size_t esz = elem_size(a.dtype);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t S = a.cache.S;
   for (int32_t i = 0; i < a.P; ++i) {
     const int64_t off = a.offsets[i], rows = a.offsets[i + 1] - a.offsets[i];
-    const uint8_t* src = static_cast<const uint8_t*>(a.cO) + static_cast<size_t>((i * a.N + off) * a.d) * esz;
+    const int64_t slot = a.cache.slot[i * a.P + i];
+    const uint8_t* src = static_cast<const uint8_t*>(a.cache.dO) +
+                         static_cast<size_t>((slot * a.N + off) * a.d) * esz;
     uint8_t* dst = static_cast<uint8_t*>(snapshot->ptr) + static_cast<size_t>(off * a.d) * esz;
     if (cudaMemcpy2DAsync(dst, static_cast<size_t>(a.N * a.d) * esz, src,
-                          static_cast<size_t>(a.P * a.N * a.d) * esz,
+                          static_cast<size_t>(S * a.N * a.d) * esz,
                           static_cast<size_t>(rows * a.d) * esz, static_cast<size_t>(a.B * a.H),
                           cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return DITANGO_ERR_CUDA;
@@ -496,12 +536,14 @@ int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
   if (out->ptr == nullptr) return DITANGO_ERR_INVALID_ARG;
   for (int a = 0; a < 3; ++a)
     if (sl->O_stride[a] % vec != 0) return DITANGO_ERR_ALIGN;
+  for (int a = 0; a < 3; ++a)
+    if (sl->O_stride[a] < 1 || sl->lse_stride[a] < 1) return DITANGO_ERR_SHAPE;
   for (int32_t s = 0; s < sl->n; ++s) {
     if (sl->O[s] == nullptr || sl->lse[s] == nullptr) return DITANGO_ERR_INVALID_ARG;
     if (!aligned16(sl->O[s])) return DITANGO_ERR_ALIGN;
   }
   if (out->dtype != sl->dtype) return DITANGO_ERR_DTYPE;
-  if (out->stride[3] != 1) return DITANGO_ERR_SHAPE;
+  if (out->stride[3] != 1 || !positive_strides(out, 3)) return DITANGO_ERR_SHAPE;
   if (!aligned16(out->ptr)) return DITANGO_ERR_ALIGN;
   for (int a = 0; a < 3; ++a)
     if (out->stride[a] % vec != 0) return DITANGO_ERR_ALIGN;
@@ -511,6 +553,7 @@ int ditango_merge(const ditango_state_list* sl, const ditango_tensor* out,
     if (out_lse->ndim != 3 || out_lse->shape[0] != G1 || out_lse->shape[1] != G2 ||
         out_lse->shape[2] != R)
       return DITANGO_ERR_SHAPE;
+    if (!positive_strides(out_lse, 3)) return DITANGO_ERR_SHAPE;
   }
   MergeArgs ma;
   std::memset(&ma, 0, sizeof(ma));
@@ -542,9 +585,12 @@ int ditango_rope_build_tables(const ditango_rope* rope, double theta, void* stre
   if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0 || ((rope->dt | rope->dh | rope->dw) & 1))
     return DITANGO_ERR_INVALID_ARG;
   if (rope->T_tab < 0 || rope->Hl < 0 || rope->Wl < 0) return DITANGO_ERR_INVALID_ARG;
-  if ((rope->dt && rope->T_tab && (!rope->cos_t || !rope->sin_t)) ||
-      (rope->dh && rope->Hl && (!rope->cos_h || !rope->sin_h)) ||
-      (rope->dw && rope->Wl && (!rope->cos_w || !rope->sin_w)))
+  if ((rope->dt && rope->T_tab &&
+       (!rope->cos_t || !rope->sin_t || !rope->cos_t_lo || !rope->sin_t_lo)) ||
+      (rope->dh && rope->Hl &&
+       (!rope->cos_h || !rope->sin_h || !rope->cos_h_lo || !rope->sin_h_lo)) ||
+      (rope->dw && rope->Wl &&
+       (!rope->cos_w || !rope->sin_w || !rope->cos_w_lo || !rope->sin_w_lo)))
     return DITANGO_ERR_INVALID_ARG;
   return launch_rope_tables(*rope, theta, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DITANGO_OK

@@ -14,10 +14,11 @@
 #include <mutex>
 
 #include "ditango_internal.h"
+#include "plan_internal.h"
 
 namespace {
 
-// 64 MiB: rotated q and k in bf16 for up to 2^24 elements each (B * N * H * d).
+// 64 MiB: rotated q and k for up to 2^24 bf16 (2^23 fp32) elements each (B * N * H * d).
 constexpr size_t kStaticWorkspaceBytes = size_t{64} << 20;
 
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
@@ -50,7 +51,15 @@ extern "C" int ditango_attn_step_static_workspace(
     const ditango_rope* rope, const uint8_t* reuse_mask, const ditango_state_cache* cache,
     const ditango_tensor* out, const ditango_tensor* out_lse, float softmax_scale, void* stream) {
   if (plan == nullptr || q == nullptr) return DITANGO_ERR_INVALID_ARG;
-  if (q->ndim != 4) return DITANGO_ERR_SHAPE;  // as ditango_attn_step reports it
+  // the shape checks ditango_attn_step makes before it looks at the workspace, so that a bad
+  // shape is reported as SHAPE here too rather than sizing the scratch from it
+  if (q->ndim != 4) return DITANGO_ERR_SHAPE;
+  for (int a = 0; a < 4; ++a)
+    if (q->shape[a] < 1) return DITANGO_ERR_SHAPE;
+  if (q->shape[1] != plan->N) return DITANGO_ERR_SHAPE;
+  if (static_cast<double>(q->shape[0]) * static_cast<double>(q->shape[1]) *
+          static_cast<double>(q->shape[2]) > 2147483648.0)
+    return DITANGO_ERR_SHAPE;
   const size_t need = ditango_attn_step_workspace_size(plan, q->shape[0], q->shape[2],
                                                        static_cast<int32_t>(q->shape[3]), q->dtype,
                                                        rope != nullptr ? 1 : 0);

@@ -30,6 +30,41 @@ struct PairSchedule {
   int32_t seg_start[kMaxP + 1];  // first unit of order[k]; seg_start[P] = n_units
 };
 
+// Where the states of a layer's state cache live. The device cache holds S slots per query
+// row ([B, H, S, N, d] and [B, H, S, N]); pair (i, j) with slot[i * P + j] = s >= 0 lives in
+// device slot s, every other pair in slot j of the host cache ([B, H, P, N, d] and
+// [B, H, P, N], page-locked host memory addressed by the device). Without host storage S = P
+// and slot[i * P + j] = j.
+struct CacheLoc {
+  void* dO;
+  float* dL;
+  void* hO;
+  float* hL;
+  int32_t S;
+  int8_t slot[kMaxP * kMaxP];
+};
+
+// O and lse pointers of the state (i, j) of query row r of (b, h) slab bh (d channels of T).
+template <typename T>
+__host__ __device__ __forceinline__ void state_ptrs(const CacheLoc& c, int32_t P, int64_t N,
+                                                    int32_t d, int64_t bh, int32_t i, int32_t j,
+                                                    int64_t r, T*& o, float*& l) {
+  const int s = c.slot[i * P + j];
+  if (s >= 0) {
+    const int64_t row = (bh * c.S + s) * N + r;
+    o = static_cast<T*>(c.dO) + row * d;
+    l = c.dL + row;
+  } else {
+    const int64_t row = (bh * P + j) * N + r;
+    o = static_cast<T*>(c.hO) + row * d;
+    l = c.hL + row;
+  }
+}
+
+// Device slot of every pair when the device cache holds S of the P states per row (host only;
+// the rule of ditango_cache_slot_map).
+void cache_slot_map(int32_t P, int32_t S, int8_t* map);
+
 // Fills a schedule. `mask` is P*P (1 = reuse). Host only.
 void build_schedule(int64_t N, int32_t P, const int64_t* offsets, const uint8_t* mask, int64_t B,
                     int64_t H, int32_t block_rows, PairSchedule* s);
@@ -40,6 +75,7 @@ void build_schedule(int64_t N, int32_t P, const int64_t* offsets, const uint8_t*
 // Wl rows of stride sW (strides in pairs, odd so that a warp's 32 rows hit distinct banks).
 struct RopeQ {
   const float *cos_t, *sin_t, *cos_h, *sin_h, *cos_w, *sin_w;
+  const float *cos_t_lo, *sin_t_lo, *cos_h_lo, *sin_h_lo, *cos_w_lo, *sin_w_lo;  // residuals
   int32_t Hl, Wl, start_frame;
   int32_t dt, dh, dw;
   int32_t nT, sT, sH, sW;
@@ -52,8 +88,7 @@ constexpr int kRopeSmemMaxBytes = 32768;
 struct PairTcArgs {
   PairSchedule sched;
   int64_t N;
-  void* cache_O;      // bf16 [B, H, P, N, d]
-  float* cache_lse;   // [B, H, P, N]
+  CacheLoc cache;     // bf16 states
   float scale_log2;   // softmax scale * log2(e)
   int* err;           // device error word
   RopeQ rope;         // rotation applied to each Q tile after it lands in shared memory
@@ -69,8 +104,7 @@ struct PairF32Args {
   int64_t N;
   const float* q; const float* k; const float* v;
   int64_t qs[3], ks[3], vs[3];  // element strides of b, n, h (d contiguous)
-  float* cache_O;     // [B, H, P, N, d]
-  float* cache_lse;   // [B, H, P, N]
+  CacheLoc cache;     // fp32 states
   float scale;
 };
 cudaError_t launch_pair_f32(int d, const PairF32Args& args, cudaStream_t stream);
@@ -94,17 +128,19 @@ cudaError_t launch_merge(const MergeArgs& args, cudaStream_t stream);
 
 // The merge of one attention step: every query row r of partition i merges the cache states
 // (i, j) of the pairs in cache_set[i] and, if bit i of `group` is set, the group state of its
-// row (the composed state of partition i's reused pairs).
+// row (the composed state of partition i's reused pairs). If bit i of `rebuild` is set, the
+// row first builds that group state from the cache states in reused_set[i] and stores it.
 struct StepMergeArgs {
   int32_t P, d, dtype;  // dtype of the cache states and of out
   int64_t B, H, N;
   int32_t offsets[kMaxP + 1];
   uint64_t cache_set[kMaxP];
-  uint64_t group;
-  const void* cO;   // [B, H, P, N, d]
-  const float* cL;  // [B, H, P, N]
-  const float* gO;  // [B, H, N, d] fp32 (may be null when group == 0)
-  const float* gL;  // [B, H, N]
+  uint64_t reused_set[kMaxP];
+  uint64_t group;    // partitions whose rows start from their group state
+  uint64_t rebuild;  // partitions whose group state is built in this launch (subset of group)
+  CacheLoc cache;
+  float* gO;        // [B, H, N, d] fp32 (may be null when group == 0)
+  float* gL;        // [B, H, N]
   void* out;        // element strides of b, h, r in outS (d contiguous)
   int64_t outS[3];
   float* out_lse;   // may be null
@@ -119,8 +155,7 @@ struct PlannerArgs {
   int32_t P, d, dtype;  // dtype of the cache O and the snapshot
   int64_t B, H, N;
   int32_t offsets[kMaxP + 1];
-  const float* cL;   // cache lse [B, H, P, N]
-  const void* cO;    // cache O [B, H, P, N, d]
+  CacheLoc cache;
   const void* snap;  // diagonal states at the anchor [B, H, N, d]
   double* sums;      // device scratch: P*P (importance) or 2P (drift) doubles
   double* out;       // device: w [P*P] or delta [P]
@@ -138,6 +173,7 @@ struct RopeApplyArgs {
   int64_t B, N, H;
   int32_t d;
   const float *cos_t, *sin_t, *cos_h, *sin_h, *cos_w, *sin_w;
+  const float *cos_t_lo, *sin_t_lo, *cos_h_lo, *sin_h_lo, *cos_w_lo, *sin_w_lo;  // residuals
   int64_t Hl, Wl, start_frame;
   int32_t dt, dh, dw;
 };

@@ -11,11 +11,11 @@
 // Thread layout: grid.y walks the row groups (a (b, h) slab; launched in chunks of at most
 // 65535), grid.x the rows of a group; each row is handled by d/VEC consecutive threads, each
 // owning VEC contiguous channels loaded as one 16-byte vector per state, so a warp reads whole
-// rows of every state in fully used 32-byte sectors. Index arithmetic is 32-bit shifts and
-// masks (d/VEC is a power of two); exponentials and the logarithm use the SFU approximations
-// (relative error ~2^-22). States are merged online in rounds (eight for a state list, two for
-// a step) whose vectors and lse values are all loaded before any is used (a short round repeats
-// a state with weight 0), so a round costs one memory round trip.
+// rows of every state in fully used 32-byte sectors. Index arithmetic is 32-bit (shifts and
+// masks when d/VEC is a power of two, a division otherwise); exponentials and the logarithm use
+// the SFU approximations (relative error ~2^-22). States are merged online in rounds whose
+// vectors and lse values are all loaded before any is used, so a round costs one memory round
+// trip: eight states per round for a state list, two for a step (see launch_step_typed).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -85,73 +85,141 @@ __device__ __forceinline__ void unpack(const uint4& v, float (&x)[8], const __nv
   }
 }
 
-// Online merge of one round of up to kRound states (the rest of the round repeats an earlier
-// state with use = false): raw[q] and l[q] (lse in log2 units) were loaded together, so the
-// whole round is one memory round trip. acc and sum are relative to the running max mx.
-template <typename T, int VEC, int kRound>
-__device__ __forceinline__ void merge_round(const uint4 (&raw)[kRound], const float (&l)[kRound],
-                                            const bool (&use)[kRound], float& mx, float& sum,
-                                            float (&acc)[VEC]) {
+// A row's view of the state cache: where state j of the row lives (device or host slot).
+struct RowStates {
+  const CacheLoc* c;
+  int32_t P, d, i;
+  int64_t N, bh, r;
+  int c0;
+  template <typename T>
+  __device__ __forceinline__ void ptrs(int j, const T*& o, const float*& l) const {
+    T* op;
+    float* lp;
+    state_ptrs(*c, P, N, d, bh, i, j, r, op, lp);
+    o = op + c0;
+    l = lp;
+  }
+};
+
+// Loads the next round of up to NS states of `m` (a bit set of states j, lowest first): the
+// 16-byte vector of this thread's channels and the lse (log2 units) of each, all issued before
+// any is used, so that a round costs one memory round trip. Slots past the set get lse = -inf
+// and a zero vector. Returns how many states were loaded; m loses their bits.
+template <typename T, int NS>
+__device__ __forceinline__ int load_round(uint64_t& m, const RowStates& rs, uint4 (&raw)[NS],
+                                          float (&l)[NS]) {
+  int cnt = 0;
+#pragma unroll
+  for (int q = 0; q < NS; ++q) {
+    if (m != 0) {
+      const int j = __ffsll(static_cast<long long>(m)) - 1;
+      m &= m - 1;
+      const T* o;
+      const float* lp;
+      rs.ptrs<T>(j, o, lp);
+      raw[q] = load_raw(o);
+      l[q] = __ldg(lp) * kLog2e;
+      ++cnt;
+    } else {
+      raw[q] = make_uint4(0u, 0u, 0u, 0u);
+      l[q] = -INFINITY;
+    }
+  }
+  return cnt;
+}
+
+// Online merge of one loaded round into (mx, sum, acc), all relative to the running max mx
+// (log2 units): acc and sum are rescaled by 2^(mx - mx_new) once per round.
+template <typename T, int VEC, int NS>
+__device__ __forceinline__ void merge_round(const uint4 (&raw)[NS], const float (&l)[NS], int cnt,
+                                            float& mx, float& sum, float (&acc)[VEC]) {
   float mn = mx;
 #pragma unroll
-  for (int q = 0; q < kRound; ++q) mn = fmaxf(mn, l[q]);
-  const float sc = ex2(mx - mn);  // 0 on the first round (mx = -inf)
+  for (int q = 0; q < NS; ++q) mn = fmaxf(mn, l[q]);
+  const float sc = ex2(mx - mn);  // 0 on the first round (mx = -inf); cnt >= 1 keeps mn finite
   sum *= sc;
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] *= sc;
 #pragma unroll
-  for (int q = 0; q < kRound; ++q) {
-    const float w = use[q] ? ex2(l[q] - mn) : 0.f;
-    sum += w;
-    float x[VEC];
-    unpack(raw[q], x, static_cast<const T*>(nullptr));
+  for (int q = 0; q < NS; ++q) {
+    if (q < cnt) {
+      const float w = ex2(l[q] - mn);
+      sum += w;
+      float x[VEC];
+      unpack(raw[q], x, static_cast<const T*>(nullptr));
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+    }
   }
   mx = mn;
 }
 
-// Row and first channel of this thread; false past the group's last row.
-__device__ __forceinline__ bool thread_row(int64_t R, int d, int vec_shift, uint32_t& r, int& c0) {
-  const int tpr_shift = 31 - __clz(d) - vec_shift;  // log2(d / VEC)
+// Merges every state of the bit set `set` (states j of this row) into (mx, sum, acc).
+template <typename T, int VEC, int NS>
+__device__ __forceinline__ void merge_set(uint64_t set, const RowStates& rs, float& mx, float& sum,
+                                          float (&acc)[VEC]) {
+  for (uint64_t m = set; m != 0;) {
+    uint4 raw[NS];
+    float l[NS];
+    const int cnt = load_round<T, NS>(m, rs, raw, l);
+    merge_round<T, VEC, NS>(raw, l, cnt, mx, sum, acc);
+  }
+}
+
+// Row and first channel of this thread (tpr = d / VEC threads per row; tpr_shift = log2(tpr)
+// when tpr is a power of two, else -1); false past the last of R rows.
+__device__ __forceinline__ bool thread_row(int64_t R, int tpr, int tpr_shift, int vec_shift,
+                                           uint32_t& r, int& c0) {
   const uint32_t t = blockIdx.x * kMergeThreads + threadIdx.x;
-  r = t >> tpr_shift;
-  c0 = static_cast<int>(t & ((1u << tpr_shift) - 1u)) << vec_shift;
+  if (tpr_shift >= 0) {
+    r = t >> tpr_shift;
+    c0 = static_cast<int>(t & ((1u << tpr_shift) - 1u)) << vec_shift;
+  } else {
+    r = t / static_cast<uint32_t>(tpr);
+    c0 = static_cast<int>(t - r * static_cast<uint32_t>(tpr)) << vec_shift;
+  }
   return r < static_cast<uint64_t>(R);
 }
 
-// merge_kernel: state list with a common [G1, G2, R, d] layout (MergeArgs). T: the states'
-// dtype, TO: the output's (T, or fp32 for group states).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// merge_kernel: state list with a common [G1, G2, R, d] layout (MergeArgs), d any multiple of
+// VEC. T: the states' dtype, TO: the output's (T, or fp32).
 template <typename T, typename TO>
 __global__ void __launch_bounds__(kMergeThreads)
-    merge_kernel(const __grid_constant__ MergeArgs a, int64_t g_base) {
+    merge_kernel(const __grid_constant__ MergeArgs a, int64_t g_base, int tpr_shift) {
   constexpr int VEC = 16 / sizeof(T);
   constexpr int VEC_SHIFT = VEC == 8 ? 3 : 2;
+  constexpr int NS = 8;  // a list of up to eight states in one round trip
   uint32_t r;
   int c0;
-  if (!thread_row(a.R, a.d, VEC_SHIFT, r, c0)) return;
+  if (!thread_row(a.R, a.d / VEC, tpr_shift, VEC_SHIFT, r, c0)) return;
   const int64_t g = g_base + blockIdx.y;
   const int64_t g1 = g / a.G2, g2 = g - g1 * a.G2;
   const int64_t lo = g1 * a.lS[0] + g2 * a.lS[1] + r * a.lS[2];
   const int64_t oo = g1 * a.oS[0] + g2 * a.oS[1] + r * a.oS[2] + c0;
 
-  constexpr int kRound = 8;  // a whole list of up to eight states in one round trip
   float mx = -INFINITY, sum = 0.f;
   float acc[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < a.n; s0 += kRound) {
-    uint4 raw[kRound];
-    float l[kRound];
-    bool use[kRound];
+  for (int s0 = 0; s0 < a.n; s0 += NS) {
+    uint4 raw[NS];
+    float l[NS];
+    const int cnt = min(NS, a.n - s0);
 #pragma unroll
-    for (int q = 0; q < kRound; ++q) {
-      use[q] = s0 + q < a.n;
-      const int s = use[q] ? s0 + q : s0;
-      raw[q] = load_raw(static_cast<const T*>(a.O[s]) + oo);
-      l[q] = __ldg(a.lse[s] + lo) * kLog2e;
+    for (int q = 0; q < NS; ++q) {
+      if (q < cnt) {
+        raw[q] = load_raw(static_cast<const T*>(a.O[s0 + q]) + oo);
+        l[q] = __ldg(a.lse[s0 + q] + lo) * kLog2e;
+      } else {
+        raw[q] = make_uint4(0u, 0u, 0u, 0u);
+        l[q] = -INFINITY;
+      }
     }
-    merge_round<T, VEC, kRound>(raw, l, use, mx, sum, acc);
+    merge_round<T, VEC, NS>(raw, l, cnt, mx, sum, acc);
   }
   const float lse = (mx + lg2(sum)) * kLn2;
   const float inv = 1.f / sum;
@@ -165,55 +233,58 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (a.out_lse != nullptr && c0 == 0) a.out_lse[g1 * a.olS[0] + g2 * a.olS[1] + r * a.olS[2]] = lse;
 }
 
-// step_merge_kernel: the merge that ends a step (StepMergeArgs). Row r of (b, h) = grid.y
-// merges the cache slots (b, h, j, r) for j in cache_set[partition(r)] and, if its partition
-// has one, its group state.
-template <typename T>
-__global__ void __launch_bounds__(kMergeThreads)
+// step_merge_kernel: the merge that ends a step (StepMergeArgs). Row r of (b, h) = grid.y, in
+// partition i:
+//   * if bit i of `rebuild` is set, the row first merges its reused states (reused_set[i]) into
+//     its new group state and stores it (fp32 O and lse), then continues from that state;
+//   * else if bit i of `group` is set, it starts from its stored group state;
+//   * then it merges the states (b, h, j, r) for j in cache_set[i].
+// State j of the row lives in a device slot or, when the cache keeps it in host memory, in its
+// host slot (CacheLoc).
+// Starting from a group state built here or loaded gives the same arithmetic (the same fp32
+// values), so a rebuild step and a steady step agree bit for bit on the same states.
+// NS: states per round (each round's loads are issued together).
+// At most 40 registers (six blocks of 256 threads per SM): measured 0.350 ms on the Wan-14B
+// layer's step against 0.382 ms at the compiler's 44 (five blocks); 32 (eight blocks) spills.
+template <typename T, int NS>
+__global__ void __launch_bounds__(kMergeThreads, 6)
     step_merge_kernel(const __grid_constant__ StepMergeArgs a, int64_t bh_base) {
   constexpr int VEC = 16 / sizeof(T);
   constexpr int VEC_SHIFT = VEC == 8 ? 3 : 2;
   uint32_t r;
   int c0;
-  if (!thread_row(a.N, a.d, VEC_SHIFT, r, c0)) return;
+  const int tpr_shift = 31 - __clz(a.d) - VEC_SHIFT;  // d / VEC is 8 or 16 (d = 64 or 128)
+  const bool live = thread_row(a.N, a.d / VEC, tpr_shift, VEC_SHIFT, r, c0);
+  // launched as a programmatic dependent of the pair kernel: everything below reads states it
+  // wrote, so wait for that grid to complete (a no-op for an ordinary launch)
+  grid_dependency_wait();
+  if (!live) return;
   const int64_t bh = bh_base + blockIdx.y;
   int i = 0;
   while (r >= static_cast<uint32_t>(a.offsets[i + 1])) ++i;
-  const uint64_t set = a.cache_set[i];
-  const bool grp = (a.group >> i) & 1u;
-  const float* lrow = a.cL + bh * a.P * a.N + r;  // + j * N: lse of cache state j
-  const T* orow = static_cast<const T*>(a.cO) + (bh * a.P * a.N + r) * a.d + c0;
-  const int64_t jstride = a.N * a.d;
+  const RowStates rs{&a.cache, a.P, a.d, i, a.N, bh, static_cast<int64_t>(r), c0};
 
-  // rounds of two: measured faster than rounds of four on the Wan-14B layer (0.371 vs 0.395
-  // ms: 48 instead of 62 registers, so more rows in flight per SM)
-  constexpr int kRound = 2;
-  // the group state starts the online merge (weight 1 relative to its own lse)
   float mx = -INFINITY, sum = 0.f;
   float acc[VEC];
-  if (grp) {
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  if ((a.rebuild >> i) & 1u) {
+    // Dynamic Group Compose: the reused states merge into the row's group state
+    merge_set<T, VEC, NS>(a.reused_set[i], rs, mx, sum, acc);
+    const float g_lse = (mx + lg2(sum)) * kLn2;
+    const float inv = 1.f / sum;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] *= inv;
+    store_f32<VEC>(a.gO + (bh * a.N + r) * a.d + c0, acc);
+    if (c0 == 0) a.gL[bh * a.N + r] = g_lse;
+    mx = g_lse * kLog2e;  // the group state starts the merge (weight 1 relative to its lse)
+    sum = 1.f;
+  } else if ((a.group >> i) & 1u) {
     mx = __ldg(a.gL + bh * a.N + r) * kLog2e;
     sum = 1.f;
     load_f32<VEC>(a.gO + (bh * a.N + r) * a.d + c0, acc);
-  } else {
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   }
-  for (uint64_t m = set; m;) {
-    uint4 raw[kRound];
-    float l[kRound];
-    bool use[kRound];
-    int j = __ffsll(m) - 1;
-#pragma unroll
-    for (int q = 0; q < kRound; ++q) {
-      use[q] = m != 0;
-      if (use[q]) j = __ffsll(m) - 1;  // else repeat the last state (an L1 hit)
-      m &= m - 1;
-      raw[q] = load_raw(orow + j * jstride);
-      l[q] = __ldg(lrow + j * a.N) * kLog2e;
-    }
-    merge_round<T, VEC, kRound>(raw, l, use, mx, sum, acc);
-  }
+  merge_set<T, VEC, NS>(a.cache_set[i], rs, mx, sum, acc);
   const float lse = (mx + lg2(sum)) * kLn2;
   const float inv = 1.f / sum;
 #pragma unroll
@@ -234,20 +305,45 @@ unsigned blocks_x(int64_t R, int d, int vec) {
   return static_cast<unsigned>((threads + kMergeThreads - 1) / kMergeThreads);
 }
 
+template <typename T, int NS>
+cudaError_t launch_step_chunk(const StepMergeArgs& a, dim3 grid, int64_t g0, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_merge_kernel<T, NS>, a, g0);
+}
+
+// Rounds of two states: measured faster than whole-row rounds (Wan-14B layer 0.353 ms against
+// 0.432 ms with rounds of four, 720p layer 1.08 ms against 1.74 ms with rounds of eight): fewer
+// registers per thread keep more rows in flight per SM, which matters more than the loads each
+// thread issues at once.
+template <typename T>
+cudaError_t launch_step_typed(const StepMergeArgs& a, dim3 grid, int64_t g0, cudaStream_t stream) {
+  return launch_step_chunk<T, 2>(a, grid, g0, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_step_merge(const StepMergeArgs& a, cudaStream_t stream) {
   const int vec = a.dtype == DITANGO_BF16 ? 8 : 4;
   const int64_t groups = a.B * a.H;
   if (groups == 0 || a.N == 0) return cudaSuccess;
+  if (a.d != 64 && a.d != 128) return cudaErrorInvalidValue;
   const unsigned bx = blocks_x(a.N, a.d, vec);
   if (bx == 0) return cudaErrorInvalidValue;
   for (int64_t g0 = 0; g0 < groups; g0 += kMaxGridY) {
     const dim3 grid(bx, static_cast<unsigned>(std::min<int64_t>(kMaxGridY, groups - g0)));
-    if (a.dtype == DITANGO_BF16)
-      step_merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(a, g0);
-    else
-      step_merge_kernel<float><<<grid, kMergeThreads, 0, stream>>>(a, g0);
+    const cudaError_t e = a.dtype == DITANGO_BF16
+                              ? launch_step_typed<__nv_bfloat16>(a, grid, g0, stream)
+                              : launch_step_typed<float>(a, grid, g0, stream);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -256,16 +352,19 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   const int vec = a.dtype == DITANGO_BF16 ? 8 : 4;
   const int64_t groups = a.G1 * a.G2;
   if (groups == 0 || a.R == 0) return cudaSuccess;
+  if (a.d % vec != 0) return cudaErrorInvalidValue;
   const unsigned bx = blocks_x(a.R, a.d, vec);
   if (bx == 0) return cudaErrorInvalidValue;
+  const int tpr = a.d / vec;
+  const int tpr_shift = (tpr & (tpr - 1)) == 0 ? 31 - __builtin_clz(static_cast<unsigned>(tpr)) : -1;
   for (int64_t g0 = 0; g0 < groups; g0 += kMaxGridY) {
     const dim3 grid(bx, static_cast<unsigned>(std::min<int64_t>(kMaxGridY, groups - g0)));
     if (a.dtype == DITANGO_BF16 && a.out_dtype == DITANGO_BF16)
-      merge_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(a, g0);
+      merge_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(a, g0, tpr_shift);
     else if (a.dtype == DITANGO_BF16 && a.out_dtype == DITANGO_F32)
-      merge_kernel<__nv_bfloat16, float><<<grid, kMergeThreads, 0, stream>>>(a, g0);
+      merge_kernel<__nv_bfloat16, float><<<grid, kMergeThreads, 0, stream>>>(a, g0, tpr_shift);
     else if (a.dtype == DITANGO_F32 && a.out_dtype == DITANGO_F32)
-      merge_kernel<float, float><<<grid, kMergeThreads, 0, stream>>>(a, g0);
+      merge_kernel<float, float><<<grid, kMergeThreads, 0, stream>>>(a, g0, tpr_shift);
     else
       return cudaErrorInvalidValue;
   }

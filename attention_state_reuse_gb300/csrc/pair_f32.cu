@@ -105,15 +105,16 @@ __global__ void __launch_bounds__(kRows * (D / 32))
       m_run = m_new;
     }
     if (row_ok) {
-      const size_t slot = (static_cast<size_t>(b * sch.H + h) * sch.P + j) * static_cast<size_t>(a.N) +
-                          static_cast<size_t>(r);
-      float* o = a.cache_O + slot * D + part * 32;
+      float* o;
+      float* lse_p;
+      state_ptrs(a.cache, sch.P, a.N, D, static_cast<int64_t>(b) * sch.H + h, i, j, r, o, lse_p);
+      o += part * 32;
       const float inv_l = 1.f / l_run;
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
         *reinterpret_cast<float4*>(o + e) =
             make_float4(acc[e] * inv_l, acc[e + 1] * inv_l, acc[e + 2] * inv_l, acc[e + 3] * inv_l);
-      if (part == 0) a.cache_lse[slot] = m_run + logf(l_run);
+      if (part == 0) *lse_p = m_run + logf(l_run);
     }
   }
 }

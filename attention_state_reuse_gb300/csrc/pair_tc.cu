@@ -35,6 +35,7 @@
 
 #include "ditango_internal.h"
 #include "ptx_sm103.cuh"
+#include "rope_round.cuh"
 
 namespace ditango {
 namespace {
@@ -187,6 +188,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float2 ld_shared_f2(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
@@ -223,12 +234,17 @@ __device__ __forceinline__ void stage_rope_table(const RopeQ& r, float2* tab, in
 // Encoding Using a Global Time Index", section 2). The row is D bf16 values in 128-byte lines,
 // one per 64-channel chunk, with its 16-byte units stored at unit ^ (row mod 8). Channel pair
 // m = (2m, 2m+1) turns by the angle of table entry m of the token's frame (m < dt/2), row
-// (next dh/2) or column (last dw/2), evaluated as y0 = fl(fl(x0 c) - fl(x1 s)),
-// y1 = fl(fl(x0 s) + fl(x1 c)) with fp32 multiplies and adds that are never contracted into
-// FMAs (the rotary pre-pass evaluates the same expression), then rounded to bf16. n is the
-// token's index in the sequence; tab is the staged table (shared-space address).
+// (next dh/2) or column (last dw/2); each output is the nearest-even bf16 of the rotation with
+// fp64 cos/sin, as in the rotary pre-pass (rope_round.cuh). A first pass takes the fp32 fast
+// path from the staged table and leaves the rare pairs whose rounding it cannot decide
+// unrotated, noting them in a bit mask; a second pass recomputes only those exactly, reading
+// the residual tables from global memory. Both passes are rolled loops in a function of its
+// own: the row rotation runs once per unit, and unrolled or inlined into the softmax loop it
+// cost that loop registers (measured: 5.9 ms unrolled and inlined, 5.35 ms this way, against
+// 5.2 ms for a plain fp32 rotation, on the Wan-14B layer's reuse step). n is the token's index
+// in the sequence; tab is the staged table (shared-space address).
 template <int D>
-__device__ __forceinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor, int n,
+__device__ __noinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor, int n,
                                              const RopeQ& r, uint32_t tab) {
   const int hw_tokens = r.Hl * r.Wl;
   const int tl = n / hw_tokens;
@@ -240,27 +256,51 @@ __device__ __forceinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor
   const uint32_t bt = tab + 8u * static_cast<uint32_t>(tl * r.sT);
   const uint32_t bh = tab + 8u * static_cast<uint32_t>(r.nT * r.sT + hp * r.sH - ht);
   const uint32_t bw = tab + 8u * static_cast<uint32_t>(r.nT * r.sT + r.Hl * r.sH + wp * r.sW - hth);
+  uint64_t unsure = 0;  // bit m: pair m still holds its input, to be rotated exactly below
+#pragma unroll 1
+  for (int u = 0; u < D / 8; ++u) {  // 16-byte units: chunk u / 8, unit u % 8 of the chunk
+    const uint32_t addr = row_addr + (u >> 3) * kChunkBytes + (((u & 7) ^ row_xor) << 4);
+    const uint4 v = ld_shared_v4(addr);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
 #pragma unroll
-  for (int c = 0; c < D / 64; ++c) {
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      const uint32_t addr = row_addr + c * kChunkBytes + ((x ^ row_xor) << 4);
-      const uint4 u = ld_shared_v4(addr);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int m = c * 32 + x * 4 + p;  // channel pair index
-        const uint32_t base = m < ht ? bt : (m < hth ? bh : bw);
-        const float2 cs = ld_shared_f2(base + 8u * m);
-        const float x0 = __uint_as_float(wv[p] << 16);
-        const float x1 = __uint_as_float(wv[p] & 0xFFFF0000u);
-        const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
-        const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
-        o[p] = pack_bf16x2(y0, y1);
+    for (int p = 0; p < 4; ++p) {
+      const int m = u * 4 + p;  // channel pair index
+      const uint32_t base = m < ht ? bt : (m < hth ? bh : bw);
+      const float2 cs = ld_shared_f2(base + 8u * m);
+      bool sure;
+      o[p] = rope_rotate_bf16x2_fast(__uint_as_float(wv[p] << 16),
+                                     __uint_as_float(wv[p] & 0xFFFF0000u), cs.x, cs.y, sure);
+      if (!sure) {
+        o[p] = wv[p];
+        unsure |= uint64_t{1} << m;
       }
-      st_shared_v4(addr, o[0], o[1], o[2], o[3]);
     }
+    st_shared_v4(addr, o[0], o[1], o[2], o[3]);
+  }
+  while (unsure != 0) {  // rare: about one pair in a thousand
+    const int m = __ffsll(static_cast<long long>(unsure)) - 1;
+    unsure &= unsure - 1;
+    const int u = m >> 2;
+    const uint32_t addr = row_addr + (u >> 3) * kChunkBytes + (((u & 7) ^ row_xor) << 4) + 4u * (m & 3);
+    const uint32_t w = ld_shared_u32(addr);
+    const uint32_t base = m < ht ? bt : (m < hth ? bh : bw);
+    const float2 cs = ld_shared_f2(base + 8u * m);
+    const float *pc, *ps;
+    int idx;
+    if (m < ht) {
+      idx = (r.start_frame + tl) * ht + m;
+      pc = r.cos_t_lo; ps = r.sin_t_lo;
+    } else if (m < hth) {
+      idx = hp * (r.dh >> 1) + (m - ht);
+      pc = r.cos_h_lo; ps = r.sin_h_lo;
+    } else {
+      idx = wp * (r.dw >> 1) + (m - hth);
+      pc = r.cos_w_lo; ps = r.sin_w_lo;
+    }
+    st_shared_u32(addr, rope_rotate_bf16x2_exact(__uint_as_float(w << 16),
+                                                 __uint_as_float(w & 0xFFFF0000u), cs.x, cs.y,
+                                                 __ldg(pc + idx), __ldg(ps + idx)));
   }
 }
 
@@ -569,10 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after_sync();
         const float inv_l = 1.f / l_run;
-        const size_t slot = (static_cast<size_t>(ui.b * sch.H + ui.h) * sch.P + j) *
-                                static_cast<size_t>(args.N) +
-                            static_cast<size_t>(ui.row0 + w * kTileRows + lrow);
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(args.cache_O) + slot * D;
+        // the pair's slot: a device slot, or its host slot when the cache keeps it in host
+        // memory (the stores then cross the host link)
+        __nv_bfloat16* orow;
+        float* lse_p;
+        state_ptrs(args.cache, sch.P, args.N, D, static_cast<int64_t>(ui.b) * sch.H + ui.h, ui.i, j,
+                   static_cast<int64_t>(ui.row0 + w * kTileRows + lrow), orow, lse_p);
         // read the whole row of O in one TMEM load and hand O back to the MMA warp before the
         // packing and the global stores, so that the next partition's first P V can start
         uint32_t r[D];
@@ -591,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t p3 = pack_bf16x2(__uint_as_float(r[8 * c + 6]) * inv_l, __uint_as_float(r[8 * c + 7]) * inv_l);
             reinterpret_cast<uint4*>(orow)[c] = make_uint4(p0, p1, p2, p3);
           }
-          args.cache_lse[slot] = (m_run + __log2f(l_run)) * kLn2;
+          *lse_p = (m_run + __log2f(l_run)) * kLn2;
         }
       }
     }

@@ -36,6 +36,24 @@ int check_values(int32_t P, const uint8_t* mask) {
 
 namespace ditango {
 
+// Device slots of a cache that keeps S of the P states of a row on the device: for query
+// partition i, the S pairs nearest the diagonal (smallest |i - j|, ties to the smaller j) take
+// slots 0..S-1 in ascending j; the others are kept in host memory (-1). These are the pairs a
+// distance mask computes, and the local pair (i, i) is always on the device.
+void cache_slot_map(int32_t P, int32_t S, int8_t* map) {
+  for (int32_t i = 0; i < P; ++i) {
+    std::vector<int32_t> js(P);
+    std::iota(js.begin(), js.end(), 0);
+    std::stable_sort(js.begin(), js.end(), [i](int32_t a, int32_t b) {
+      return std::abs(a - i) < std::abs(b - i);  // stable: ties keep the smaller j first
+    });
+    std::vector<uint8_t> on_dev(P, 0);
+    for (int32_t k = 0; k < S; ++k) on_dev[js[k]] = 1;
+    int8_t next = 0;
+    for (int32_t j = 0; j < P; ++j) map[i * P + j] = on_dev[j] ? next++ : int8_t{-1};
+  }
+}
+
 const uint8_t* plan_effective_mask(const ditango_plan_s* p, const uint8_t* mask) {
   return mask != nullptr ? mask : p->mask.data();
 }
@@ -302,3 +320,9 @@ int ditango_plan_set_cache_state(ditango_plan_t plan, const uint8_t* valid,
 }
 
 }  // extern "C"
+
+extern "C" int ditango_cache_slot_map(int32_t P, int32_t S, int8_t* map) {
+  if (map == nullptr || P < 1 || P > kMaxP || S < 1 || S > P) return DITANGO_ERR_INVALID_ARG;
+  ditango::cache_slot_map(P, S, map);
+  return DITANGO_OK;
+}

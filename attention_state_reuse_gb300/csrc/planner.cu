@@ -57,14 +57,20 @@ __global__ void __launch_bounds__(kThreads) importance_kernel(const __grid_const
   const int i = partition_of(a, rr);
   const int i0 = __shfl_sync(0xffffffffu, i, 0);  // every lane takes part, live or not
   const bool uniform = __all_sync(0xffffffffu, live && i == i0);
-  const float* lrow = a.cL + static_cast<int64_t>(blockIdx.y) * a.P * a.N + rr;
+  // lse of state j of the row (a device slot, or its host slot for a state kept in host memory)
+  auto lse_of = [&](int j) {
+    char* o;
+    float* l;
+    state_ptrs(a.cache, a.P, a.N, 0, static_cast<int64_t>(blockIdx.y), i, j, rr, o, l);
+    return *l;
+  };
   float mx = -INFINITY;
-  for (int j = 0; j < a.P; ++j) mx = fmaxf(mx, lrow[j * a.N]);
+  for (int j = 0; j < a.P; ++j) mx = fmaxf(mx, lse_of(j));
   float sum = 0.f;
-  for (int j = 0; j < a.P; ++j) sum += exp2f((lrow[j * a.N] - mx) * kLog2e);
+  for (int j = 0; j < a.P; ++j) sum += exp2f((lse_of(j) - mx) * kLog2e);
   const float inv = 1.f / sum;
   for (int j = 0; j < a.P; ++j) {
-    const float wj = live ? exp2f((lrow[j * a.N] - mx) * kLog2e) * inv : 0.f;
+    const float wj = live ? exp2f((lse_of(j) - mx) * kLog2e) * inv : 0.f;
     add_slot(acc, i * a.P + j, wj, uniform);
   }
   __syncthreads();
@@ -110,7 +116,13 @@ __global__ void __launch_bounds__(kThreads) drift_kernel(const __grid_constant__
   const int i0 = __shfl_sync(0xffffffffu, i, 0);  // every lane takes part, live or not
   const bool uniform = __all_sync(0xffffffffu, live && i == i0);
   const int64_t bh = blockIdx.y;
-  const T* cur = static_cast<const T*>(a.cO) + ((bh * a.P + i) * a.N + rr) * a.d;
+  const T* cur;
+  {
+    T* o;
+    float* l;
+    state_ptrs(a.cache, a.P, a.N, a.d, bh, i, i, rr, o, l);  // the local state (i, i)
+    cur = o;
+  }
   const T* ref = static_cast<const T*>(a.snap) + (bh * a.N + rr) * a.d;
   float num = 0.f, den = 0.f;
   for (int c = 0; c < a.d; c += 8) {

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define DITANGO_ABI_VERSION 2
+#define DITANGO_ABI_VERSION 3
 #define DITANGO_MAX_PARTITIONS 64 /* P limit of a plan */
 #define DITANGO_MAX_STATES 64     /* state limit of one ditango_merge call */
 
@@ -77,6 +77,20 @@ typedef struct {
  * step. O: [B, H, P, N, d], contiguous, dtype BF16 for bf16 inputs and F32 for f32 inputs.
  * lse: [B, H, P, N], contiguous, F32. Slot [b, h, j, r] holds the state of (partition(r), j)
  * for query row r. Contents are meaningful only for pairs this plan has computed.
+ * host_O, host_lse (optional: ptr NULL = not used): host storage for the states that do not
+ * fit in device memory (DiTango, closing limitations paragraph: state-cache memory is a
+ * constraint, CPU offloading is the remedy it names). With them, O and lse hold only S device
+ * slots per row ([B, H, S, N, d] and [B, H, S, N], 1 <= S <= P) and host_O, host_lse are
+ * [B, H, P, N, d] and [B, H, P, N] (same dtypes, contiguous) in page-locked host memory that
+ * the device can address (cudaHostAlloc / cudaHostRegister). For query partition i the S pairs
+ * (i, j) nearest the diagonal (smallest |i - j|, ties to the smaller j; see
+ * ditango_cache_slot_map) keep their states in device slots 0..S-1 in ascending j; every other
+ * pair keeps its state in host slot [b, h, j, r]. The kernels read and write host states in
+ * place over the host link; nothing is copied, and every result is bit-identical to a cache
+ * held wholly on the device. With group states and a distance mask |i - j| >= D, S = 2D - 1
+ * keeps every pair a steady reuse step computes on the device: host memory is then written
+ * when far pairs are computed (anchor steps) and read when group states are rebuilt. Without
+ * host storage S must equal P.
  * group_O, group_lse (optional: ptr NULL = not used): one composed state per query row,
  * [B, H, N, d] and [B, H, N], contiguous, both F32 (DiTango, Methodology 2, State Composition
  * and Dynamic Group Compose: cached states merge into a coarser group state without
@@ -91,14 +105,26 @@ typedef struct {
   ditango_tensor lse;
   ditango_tensor group_O;
   ditango_tensor group_lse;
+  ditango_tensor host_O;
+  ditango_tensor host_lse;
 } ditango_state_cache;
+
+/* Host only: where each pair's state lives when the device cache holds S of the P states per
+ * row. map (P*P bytes, row-major [i][j]) receives the device slot (0..S-1) of pair (i, j), or
+ * -1 for a pair kept in host storage. S = P maps pair (i, j) to slot j. Errors: INVALID_ARG
+ * (P outside [1, 64], S outside [1, P], NULL map). */
+int ditango_cache_slot_map(int32_t P, int32_t S, int8_t* map);
 
 /* Precomputed 3D RoPE tables (device memory, fp32, row-major, filled by
  * ditango_rope_build_tables). Channel pairs (2m, 2m+1) of each head: the first dt/2 pairs turn
  * with the global frame index t, the next dh/2 with the row h, the last dw/2 with the column w;
  * pair k of an axis of width d_a turns by pos * theta^(-2k/d_a).
  * Token n of the sequence sits at t = n / (Hl*Wl) + start_frame, h = (n / Wl) % Hl,
- * w = n % Wl, so N must be a multiple of Hl*Wl and start_frame + N/(Hl*Wl) <= T_tab. */
+ * w = n % Wl, so N must be a multiple of Hl*Wl and start_frame + N/(Hl*Wl) <= T_tab.
+ * Each table has a residual table of the same shape: cos_t_lo = fl32(cos - cos_t) with cos in
+ * fp64, and so on, so that table + residual carries cos and sin to about 48 bits. The BF16
+ * path needs them to round every rotated value as the rotation with fp64 cos/sin rounds
+ * (nearest-even); all twelve pointers of a non-empty axis must be set. */
 typedef struct {
   float* cos_t; float* sin_t; /* [T_tab, dt/2] */
   float* cos_h; float* sin_h; /* [Hl, dh/2] */
@@ -106,6 +132,9 @@ typedef struct {
   int64_t T_tab, Hl, Wl;
   int32_t dt, dh, dw;       /* even, dt + dh + dw = d */
   int64_t start_frame;      /* s: global frame index of this sequence's first frame */
+  float* cos_t_lo; float* sin_t_lo; /* residuals, shapes as above */
+  float* cos_h_lo; float* sin_h_lo;
+  float* cos_w_lo; float* sin_w_lo;
 } ditango_rope;
 
 /* A list of n states with a common layout, for ditango_merge. State s has outputs O[s]
@@ -235,12 +264,15 @@ int ditango_plan_inject_fault(ditango_plan_t plan, int32_t kind);
  *   other strides must be multiples of 8 elements and the pointers 16-byte aligned.
  *   Supported d: 64 and 128 (UNSUPPORTED otherwise). B and H must be at least 1: an empty
  *   batch returns SHAPE, whatever its pointers, and leaves the plan unchanged.
- * rope: NULL = no rotation; else q and k are rotated (in fp32, rounded to the input dtype)
- *   before attention; v is never rotated.
+ * rope: NULL = no rotation; else q and k are rotated before attention and the attention reads
+ *   them in the input dtype: for BF16 each rotated value is the nearest-even bf16 of the
+ *   rotation with fp64 cos/sin (exact up to ~2^-46 relative), for F32 the rotation evaluated
+ *   in fp32 (within a few fp32 ulps); v is never rotated.
  * reuse_mask: host P*P bytes; NULL = the plan's default mask.
  * cache: the layer's state cache (see ditango_state_cache). Pairs with mask 0 are computed
  *   from this step's inputs and overwrite their slots; pairs with mask 1 are read as cached.
- * out: [B, N, H, d], same dtype as q, d contiguous. out_lse: [B, H, N] F32, or NULL.
+ * out: [B, N, H, d], same dtype as q, d contiguous. out_lse: [B, H, N] F32 with strides of
+ *   at least 1 (SHAPE otherwise), or NULL.
  * softmax_scale: the `scale` of the pair-state definition (commonly 1/sqrt(d)).
  * workspace: device memory of at least ditango_attn_step_workspace_size(...) bytes, 256-byte
  *   aligned (may be NULL when that size is 0). Its contents need not be preserved. It holds
@@ -264,8 +296,10 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
  * without the workspace: the step's scratch (the rotated q and k when rope != NULL) lives in
  * a 64 MiB device array inside the library, held on every GPU where the library's device code
  * is loaded until the process exits. Steps whose scratch exceeds 64 MiB
- * (ditango_attn_step_workspace_size > 64 MiB, i.e. more than 2^24 bf16 elements per rotated
- * tensor) return DITANGO_ERR_WORKSPACE before launching anything. Allocates nothing (no
+ * (ditango_attn_step_workspace_size > 64 MiB, i.e. more than 2^24 bf16 or 2^23 fp32 elements
+ * per rotated tensor) return DITANGO_ERR_WORKSPACE before launching anything; shapes that
+ * ditango_attn_step refuses (a dimension below 1, N other than the plan's, B*N*H above 2^31)
+ * return DITANGO_ERR_SHAPE first. Allocates nothing (no
  * cudaMalloc/cudaFree). The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress), so make it before any stream capture on that device. Every call
  * shares the one array and it keeps the last call's contents; nothing in it needs to start
@@ -286,7 +320,9 @@ size_t ditango_attn_step_workspace_size(ditango_plan_t plan, int64_t B, int64_t 
  * Source: DiTango, Methodology 2, State Composition and Dynamic Group Compose (cached states
  * merge into coarser groups without recomputation; the result is itself a state).
  * Merges the n states of `states` row by row into out ([G1, G2, R, d], same dtype as the
- * states, d contiguous, strides free) and out_lse ([G1, G2, R] F32, or NULL). Reads only the
+ * states, d contiguous, other strides at least 1) and out_lse ([G1, G2, R] F32, strides at least
+ * 1, or NULL); the list's O and lse strides must be at least 1 too. Any d that is a multiple of
+ * the 16-byte vector (8 BF16 or 4 F32 channels) is supported. Reads only the
  * listed states. With no rows (G1, G2 or R = 0) it returns DITANGO_OK without touching memory,
  * and the data pointers may be NULL. Errors: INVALID_ARG, SHAPE, DTYPE, ALIGN (O pointers / row
  * strides of BF16 states must allow 16-byte vector access), CUDA. */
@@ -296,15 +332,19 @@ int ditango_merge(const ditango_state_list* states, const ditango_tensor* out,
 /* ---- RoPE tables -------------------------------------------------------------------------
  * Source: Causal-RoPE SP page, section 2 (frequencies precomputed into contiguous tensors, so
  * inference moves no positional data between host and GPU). Fills the six fp32 tables of
- * `rope` (caller-allocated device buffers of the sizes given there) on the device:
- * cos/sin(pos * theta^(-2k/d_a)) computed in fp64 and rounded to fp32. */
+ * `rope` and their six residual tables (caller-allocated device buffers of the sizes given
+ * there) on the device: cos/sin(pos * theta^(-2k/d_a)) computed in fp64, rounded to fp32, and
+ * the fp32 rounding of what that rounding left out. */
 int ditango_rope_build_tables(const ditango_rope* rope, double theta, void* stream);
 
 /* ---- diagnostics --------------------------------------------------------------------------- */
 
 /* Synchronises `stream`, then reports and clears the device-side error word that kernels set
  * when a bounded barrier wait gives up: DITANGO_OK or DITANGO_ERR_DEVICE_TIMEOUT (with the
- * kernel's code in *code if code != NULL), or DITANGO_ERR_CUDA. */
+ * kernel's code in *code if code != NULL), or DITANGO_ERR_CUDA.
+ * The library looks up the device addresses of its own device variables (this error word, the
+ * static workspace) once per device and keeps them; after cudaDeviceReset the process must
+ * reload the library before calling it on that device again. */
 int ditango_device_status(void* stream, int32_t* code);
 
 /* Static description of a status code. */

@@ -187,3 +187,63 @@ def test_workload_mask_fractions():
     assert (np.diag(m) == 0).all()
     np.testing.assert_array_equal(m, wl.random_mask(16, 4023))
     assert 0.3 < wl.reuse_fraction(m) < 0.6
+
+
+@pytest.mark.parametrize("P,S", [(1, 1), (4, 4), (8, 3), (16, 5), (16, 1), (64, 7), (5, 2)])
+def test_cache_slot_map_keeps_the_pairs_nearest_the_diagonal(ditango, P, S):
+    # host storage of a state cache (DiTango, closing limitations paragraph: CPU offloading of
+    # the state cache): each query partition keeps its S pairs nearest the diagonal on the
+    # device, in ascending j, and the local pair always
+    m = ditango.cache_slot_map(P, S)
+    assert m.shape == (P, P) and m.dtype == np.int8
+    for i in range(P):
+        dev = [j for j in range(P) if m[i, j] >= 0]
+        assert len(dev) == S and m[i, i] >= 0
+        assert [int(m[i, j]) for j in dev] == list(range(S))  # slots in ascending j
+        want = sorted(range(P), key=lambda j: (abs(i - j), j))[:S]
+        assert sorted(want) == dev
+        assert all(m[i, j] == -1 for j in range(P) if j not in dev)
+    if S == P:
+        np.testing.assert_array_equal(m, np.tile(np.arange(P, dtype=np.int8), (P, 1)))
+
+
+def test_cache_slot_map_distance_band(ditango):
+    # S = 2D - 1 holds every pair a |i - j| >= D mask computes
+    for P, D in [(16, 3), (8, 2), (16, 2), (4, 1)]:
+        m = ditango.cache_slot_map(P, 2 * D - 1)
+        comp = wl.distance_mask(P, D) == 0
+        assert (m[comp] >= 0).all()
+
+
+@pytest.mark.parametrize("P,S", [(4, 0), (4, 5), (65, 3), (0, 1)])
+def test_cache_slot_map_refuses_bad_sizes(ditango, P, S):
+    import ctypes
+
+    lib = ditango.load_library()
+    buf = (ctypes.c_int8 * 64)()
+    assert ditango.STATUS[lib.ditango_cache_slot_map(P, S, buf)] == "INVALID_ARG"
+    assert ditango.STATUS[lib.ditango_cache_slot_map(4, 2, None)] == "INVALID_ARG"
+
+
+@pytest.mark.parametrize("shape", [(-1, 256, 2, 64), (1, 256, 0, 64), (1, 255, 2, 64),
+                                   (1 << 20, 256, 1 << 20, 64)])
+def test_static_workspace_step_reports_bad_shapes_as_shape(ditango, shape):
+    # the step without a workspace checks the shape before sizing its scratch from it
+    import ctypes
+
+    N, P = 256, 4
+    plan = ditango.Plan(N, P)
+    lib = ditango.load_library()
+    q = _desc(ditango, (1, N, 2, 64), ditango.BF16)
+    for a in range(4):
+        q.shape[a] = shape[a]
+    cache = ditango.StateCache(_desc(ditango, (1, 2, P, N, 64), ditango.BF16),
+                               _desc(ditango, (1, 2, P, N), ditango.F32))
+    out = _desc(ditango, (1, N, 2, 64), ditango.BF16)
+    rope = ditango.Rope()
+    st = lib.ditango_attn_step_static_workspace(plan.handle, ctypes.byref(q), ctypes.byref(q),
+                                                ctypes.byref(q), ctypes.byref(rope), None,
+                                                ctypes.byref(cache), ctypes.byref(out), None,
+                                                ctypes.c_float(0.125), None)
+    assert ditango.STATUS[st] == "SHAPE"
+    assert plan.cache_state()[2] == 0
