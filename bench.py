@@ -1,20 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark: one attention-layer step of partitioned attention with attention-state reuse.
 
-Workload (default): the Wan2.1-14B-shaped layer - B=1, H=40, d=128, bf16, N=32760 tokens
-(21x30x52 latent), P=8 contiguous partitions, 3D RoPE (t/h/w split 44/42/42) with a global
-time index, per-head input scales U(0.5, 2); the timed step reuses every pair with |i-j| >= 2
-(42 of 64 pairs) after an all-compute anchor step filled the state cache. A step is one call
-of ditango_attn_step: RoPE of k (q is rotated inside the pair kernel), fresh states of the 22
-computed pairs, merge of all 8 states of every row. Inputs are synthetic (seeded) and resident in HBM before timing;
-they are larger than L2 (335 MB per tensor), so no L2 flush is needed between steps.
+Workload (default): the long 720p-shaped layer - B=1, H=40, d=128, bf16, N=75600 tokens
+(21x45x80 latent), P=16 contiguous partitions, 3D RoPE (t/h/w split 44/42/42) with a global
+time index; the timed step reuses every pair with |i-j| >= 3 (182 of 256 pairs) after an
+all-compute anchor step filled the state cache. A step is one call of ditango_attn_step: RoPE of
+k (q is rotated inside the pair kernel), fresh states of the 74 computed pairs, merge of every
+row's computed states with its group state (the composed state of its reused pairs). Inputs are
+synthetic (seeded) and resident in HBM before timing; they are larger than L2 (774 MB per
+tensor), so no L2 flush is needed between steps. `--workload wan14b_layer` times the
+Wan2.1-14B-shaped layer (N=32760, P=8) instead.
 
 Prints one JSON line: ms per step (lower is better) plus effective TFLOP/s counted over
-computed pairs only, the pair kernel's roofline against measured tensor-core peak, per-kernel
+computed pairs only, the pair kernel's roofline against the measured tensor-core peak, per-kernel
 times, an end-to-end number with host buffers, clocks, and the CPU oracle baseline.
 
-`--impl reference` times the CPU oracle instead (a bounded sample of rows per step,
-extrapolated to the full step) and prints the same line with "impl": "reference".
+With --gpus N (under torchrun) the layer's heads are split across the ranks: rank r computes
+heads [r*H/N, (r+1)*H/N) of the same layer (every (b, h) is independent, so no data crosses
+ranks) and the line reports the whole layer's step time, the maximum over ranks.
+
+`--impl reference` times the CPU oracle instead (a fixed sample of rows per step, extrapolated
+to the full step) and prints the same line with "impl": "reference".
 """
 from __future__ import annotations
 
@@ -82,11 +88,14 @@ def src_hash(paths):
 
 
 PAIR_SRC = ["attention_state_reuse_gb300/csrc/pair_tc.cu",
-            "attention_state_reuse_gb300/csrc/ptx_sm103.cuh"]
+            "attention_state_reuse_gb300/csrc/ptx_sm103.cuh",
+            "attention_state_reuse_gb300/csrc/rope_round.cuh"]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per pair-kernel launch from a committed ncu summary, if it still applies."""
+def profiled_traffic(workload, heads):
+    """DRAM bytes per pair-kernel launch from a committed ncu summary, if it still applies:
+    same kernel sources and workload; scaled from the captured head count to `heads` (every
+    (b, h) reads its own q, k, v once and writes its own states)."""
     p = os.path.join(ROOT, "profiles", "pair_tc_traffic.json")
     if not os.path.exists(p):
         return None
@@ -94,7 +103,8 @@ def profiled_traffic(workload):
         rec = json.load(f)
     if rec.get("src_sha") != src_hash(PAIR_SRC) or rec.get("workload") != workload:
         return None
-    return rec.get("traffic_bytes_per_launch")
+    per_head = rec.get("traffic_bytes_per_head")
+    return None if per_head is None else int(round(per_head * heads))
 
 
 class ClockSampler:
@@ -157,6 +167,39 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# dense bf16 tcgen05 rate of one SM: a 128x128x16 MMA (2^19 flops) every 64 cycles, measured
+# with MMAs issued back to back on this GPU
+DENSE_BF16_FLOP_PER_CLK_SM = 8192
+
+
+def head_range(rank, world, H):
+    """Heads [h0, h1) that rank `rank` computes when the layer's H heads are split over `world`
+    ranks: contiguous ranges, the first H mod world ranks one head longer."""
+    base, extra = divmod(H, world)
+    h0 = rank * base + min(rank, extra)
+    return h0, h0 + base + (1 if rank < extra else 0)
+
+
+def mask_name(w):
+    kind = w.schedule[1]
+    return f"|i-j|>={kind[1]}" if kind[0] == "dist" else kind[0]
+
+
+def config_of(w, world):
+    """The `config` of the JSON line (the same for both arms)."""
+    import numpy as np
+
+    from attention_state_reuse_gb300 import workloads as wl
+
+    esz = 2 if w.dtype == "bf16" else 4
+    tensor_mb = w.B * w.N * w.H * w.d * esz / 1e6
+    return {"workload": w.name, "B": w.B, "N": w.N, "H": w.H, "d": w.d, "P": w.P,
+            "latent": [w.T, w.Hl, w.Wl], "rope": w.rope, "reuse_mask": mask_name(w),
+            "reuse_fraction": round(float(np.asarray(wl.step_mask(w, 1)).mean()), 4),
+            "parallelism": "1 GPU" if world == 1 else f"heads split over {world} GPUs",
+            "l2": f"inputs larger than L2 ({tensor_mb:.0f} MB per tensor); no flush"}
+
+
 # ------------------------------------------------------------------------------ our library
 def run_ours(args, w, rank, world):
     import numpy as np
@@ -169,9 +212,11 @@ def run_ours(args, w, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     dtype = wl.torch_dtype(w)
-    B, N, H, d, P = w.B, w.N, w.H, w.d, w.P
+    # this rank's heads of the layer (all of them on one GPU)
+    h0, h1 = head_range(rank, world, w.H)
+    B, N, H, d, P = w.B, w.N, h1 - h0, w.d, w.P
     stream = wl.InputStream(w)
-    q_np, k_np, v_np = stream.next()
+    q_np, k_np, v_np = (np.ascontiguousarray(a[:, :, h0:h1]) for a in stream.next())
     to_dev = lambda a: torch.from_numpy(a).to(dev).to(dtype)
     q, k, v = to_dev(q_np), to_dev(k_np), to_dev(v_np)
     plan = dt.Plan(N, P)
@@ -307,43 +352,58 @@ def run_ours(args, w, rank, world):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     esz = 2 if dtype == torch.bfloat16 else 4
-    h2d = 3 * B * N * H * d * esz
-    d2h = B * N * H * d * esz + B * H * N * 4
+    # bytes of the whole job (every rank copies its own heads)
+    h2d = 3 * B * N * w.H * d * esz
+    d2h = B * N * w.H * d * esz + B * w.H * N * 4
 
     sweep = reuse_sweep(dev, use_group=args.group) if (args.sweep and world == 1) else None
+    offload = offload_cycle(w, q, k, v, dev) if (args.offload and world == 1) else None
 
-    flops = pair_flops(w, mask)
+    flops = pair_flops(w, mask)            # the whole layer
+    flops_rank = flops * H / w.H           # this rank's heads
     peaks, peak_src = load_peaks()
-    tc_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     tc_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    achieved = flops / (pair_ms * 1e-3) / 1e12
-    mbytes = merge_bytes(w, mask, args.group)
+    tc_sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    achieved = flops_rank / (pair_ms * 1e-3) / 1e12
+    mbytes = merge_bytes(w, mask, args.group) * H / w.H
     merge_gbs = mbytes / (merge_ms * 1e-3) / 1e9
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     ck = clocks.summary(wall0, wall1)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = ck["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
+    med_mhz = ck["sm_mhz"] or max_mhz
+    dense = lambda mhz: n_sm * DENSE_BF16_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+    timed_s = total_ms / 1e3
     line = {
         "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
-        "data": "synthetic (seeded N(0,1) inputs, per-head scales U(0.5,2); no weights)",
-        "config": {"workload": w.name, "B": B, "N": N, "H": H, "d": d, "P": P,
-                   "latent": [w.T, w.Hl, w.Wl], "rope": w.rope, "reuse_mask": f"|i-j|>={w.schedule[1][1]}" if w.schedule[1][0] == "dist" else w.schedule[1][0],
-                   "reuse_fraction": round(float(np.asarray(mask).mean()), 4),
-                   "l2": "inputs larger than L2 (335 MB per tensor); no flush"},
-        "effective_tflops": round(world * flops / (ms * 1e-3) / 1e12, 2),  # all ranks
+        "scaling": "strong", "vs_baseline": None,
+        "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) inputs" + (", per-head scales U(0.5,2)" if w.head_scales
+                                                     else "") + "; no weights)",
+        "config": config_of(w, world),
+        "effective_tflops": round(flops / (ms * 1e-3) / 1e12, 2),  # the whole layer
         "pair_flops_per_step": flops,
+        "heads_per_rank": H,
         "kernel_ms": {"rope": round(rope_ms, 4), "pair": round(pair_ms, 4),
                       "merge": round(merge_ms, 4)},
         "anchor_ms": round(statistics.median(anchor_ms), 4),
         "first_reuse_step_ms": round(first_reuse_ms, 4),
         "group_states": bool(args.group),
         "anchor_effective_tflops": round(pair_flops(w, anchor) / (statistics.median(anchor_ms) * 1e-3) / 1e12, 2),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4),
-                     "traffic": profiled_traffic(w.name),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_burst,
+                     "unit": "TFLOP/s", "frac": round(achieved / tc_burst, 4),
+                     "traffic": profiled_traffic(w.name, H),
                      "kernel": "pair_tc_kernel<128>",
-                     "peak_source": f"bf16_tflops_sustained of {peak_src}",
-                     "frac_of_burst": round(achieved / tc_burst, 4)},
+                     "peak_source": (f"bf16_tflops (burst) of {peak_src}: the timed region lasts "
+                                     f"{timed_s:.2f} s at a {med_mhz:.0f} MHz median SM clock"),
+                     "frac_of_sustained": round(achieved / tc_sustained, 4),
+                     "dense_peak_at_median_clock": round(dense(med_mhz), 1),
+                     "frac_of_dense_at_median_clock": round(achieved / dense(med_mhz), 4),
+                     "dense_peak_at_max_clock": round(dense(max_mhz), 1),
+                     "frac_of_dense_at_max_clock": round(achieved / dense(max_mhz), 4),
+                     "dense_rate": f"{n_sm} SMs x {DENSE_BF16_FLOP_PER_CLK_SM} bf16 flop/clk "
+                                   "(a 128x128x16 tcgen05.mma every 64 cycles, measured)"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": hbm,
                            "unit": "GB/s", "frac": round(merge_gbs / hbm, 4),
                            "frac_of_8tbs": round(merge_gbs / 8000.0, 4),
@@ -353,9 +413,72 @@ def run_ours(args, w, rank, world):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": world * K * (3 if w.rope else 2),  # all ranks
         "reuse_sweep": sweep,
+        "host_storage": offload,
         "clocks": ck,
     }
     return line
+
+
+def offload_cycle(w, q, k, v, dev, cycles=2):
+    """The workload's step schedule with the far pairs' states in host memory.
+
+    The device cache keeps S = 2D - 1 slots per row (D: the schedule's reuse distance), the
+    pairs a steady step computes; the other states live in page-locked host memory and are
+    written there by the anchor steps and read back by the group-state rebuilds. Times one
+    schedule cycle (anchor, first reuse step, steady reuse steps) after a warm-up cycle, and
+    reports the device bytes of the cache with and without host storage.
+    """
+    import numpy as np
+    import torch
+
+    import attention_state_reuse_gb300 as dt
+    from attention_state_reuse_gb300 import workloads as wl
+
+    kind = w.schedule[1]
+    if kind[0] != "dist":
+        return None
+    D = kind[1]
+    B, N, H, d, P = w.B, w.N, q.shape[2], w.d, w.P
+    S = min(P, 2 * D - 1)
+    dtype = q.dtype
+    plan = dt.Plan(N, P)
+    cO, cL = dt.new_state_cache(B, H, S, N, d, dtype, dev)
+    host = dt.new_host_states(B, H, P, N, d, dtype)
+    group = dt.new_group_state(B, H, N, d, dev)
+    out = torch.empty_like(q)
+    out_lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    rope = None
+    if w.rope:
+        dtt, dhh, dww = w.rope_dims
+        rope = dt.RopeTables(w.start_frame + w.T, w.Hl, w.Wl, dtt, dhh, dww,
+                             start_frame=w.start_frame, device=dev)
+    ws = torch.empty(max(1, dt.workspace_size(plan, B, H, d, dtype, w.rope)), dtype=torch.uint8,
+                     device=dev)
+    sched = [wl.step_mask(w, t) for t in range(len(w.schedule))]
+    period = next((t for t in range(1, len(sched)) if not sched[t].any()), len(sched))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(period + 1)]
+    times = []
+    for c in range(cycles):
+        ev[0].record()
+        for t in range(period):
+            dt.attn_step(plan, q, k, v, cO, cL, out, out_lse, reuse_mask=sched[t], rope=rope,
+                         softmax_scale=w.scale, workspace=ws, group=group, host=host)
+            ev[t + 1].record()
+        torch.cuda.synchronize()
+        times = [ev[t].elapsed_time(ev[t + 1]) for t in range(period)]
+    st = dt.device_status()
+    if st != (0, 0):
+        raise RuntimeError(f"device status after the host-storage cycle: {st}")
+    esz = 2 if dtype == torch.bfloat16 else 4
+    per_slot = B * H * N * (d * esz + 4)
+    return {"device_slots_per_row": S, "partitions": P,
+            "cache_device_bytes_resident": P * per_slot,
+            "cache_device_bytes_with_host_storage": S * per_slot,
+            "device_bytes_saved": (P - S) * per_slot,
+            "host_bytes": P * per_slot,
+            "anchor_ms": round(times[0], 4), "first_reuse_step_ms": round(times[1], 4),
+            "steady_step_ms": round(statistics.median(times[2:]), 4) if period > 2 else None,
+            "schedule": f"anchor every {period} steps, |i-j|>={D} reused"}
 
 
 def reuse_sweep(dev, steps=10, use_group=True):
@@ -453,27 +576,21 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
-def replica_workload(w, rank):
-    """Rank r runs its own replica of the layer: same shapes, inputs seeded from config index
-    c + 100 r (weak scaling; no data crosses ranks)."""
-    import copy
-
-    r = copy.deepcopy(w)
-    r.index += 100 * rank
-    return r
-
-
 # ------------------------------------------------------------------------------ CPU oracle
+SAMPLE_ROWS = 2048  # query rows of head 0 the oracle computes per timed step
+
+
 class OracleBaseline:
-    """Times the CPU oracle on a bounded sample of the reuse step, extrapolated to a full step.
+    """Times the CPU oracle on a fixed sample of the reuse step, extrapolated to a full step.
 
     Sample: head 0 only; RoPE of that head's q and k over all N tokens, then the fresh states
-    of the computed pairs and the merge of all P states for `rows` query rows spread evenly
+    of the computed pairs and the merge of all P states for SAMPLE_ROWS query rows spread evenly
     over the sequence. Full-step estimate = t_rope * H * B + t_rows * (B * H * N / rows).
-    The anchor step that fills the sample's state cache runs once, untimed.
+    The anchor step that fills the sample's state cache runs once, untimed. Both arms of the
+    benchmark (the CPU baseline of ours, and --impl reference) use this same sample.
     """
 
-    def __init__(self, w, budget_s, nthreads=None):
+    def __init__(self, w, nthreads=None):
         import numpy as np
 
         import oracle
@@ -488,26 +605,13 @@ class OracleBaseline:
             dtt, dhh, dww = w.rope_dims
             self.rope_cfg = dict(Hl=w.Hl, Wl=w.Wl, start_frame=w.start_frame, dt=dtt, dh=dhh,
                                  dw=dww)
-        self.rnd = oracle.ROUND_BF16 if w.dtype == "bf16" else oracle.ROUND_F32
-        probe = max(self.nthreads, 16)
-        self._setup(probe)
-        t_rope, t_rows = self.time_step()
-        per_row = t_rows / probe
-        self.rows_n = int(max(self.nthreads, min(w.N, (budget_s - t_rope) / max(per_row, 1e-6))))
-        self._setup(self.rows_n)
-
-    def _setup(self, rows_n):
-        import numpy as np
-
-        import oracle
-
-        w = self.w
-        rows = [(0, 0, int(r)) for r in np.linspace(0, w.N - 1, rows_n).astype(np.int64)]
+        rnd = oracle.ROUND_BF16 if w.dtype == "bf16" else oracle.ROUND_F32
+        self.rows_n = min(w.N, SAMPLE_ROWS)
+        rows = [(0, 0, int(r)) for r in np.linspace(0, w.N - 1, self.rows_n).astype(np.int64)]
         self.orc = oracle.OracleRun(w.B, w.N, 1, w.d, w.P, w.scale, rows=rows,
-                                    cache_round=self.rnd, input_round=self.rnd,
-                                    rope=self.rope_cfg, nthreads=self.nthreads)
+                                    cache_round=rnd, input_round=rnd, rope=self.rope_cfg,
+                                    nthreads=self.nthreads)
         self.orc.step(self.q, self.k, self.v)  # anchor, untimed
-        self.cur_rows = rows_n
 
     def time_step(self):
         t0 = time.perf_counter()
@@ -525,47 +629,52 @@ class OracleBaseline:
     def estimate_ms(self):
         w = self.w
         t_rope, t_rows = self.time_step()
-        est = (t_rope * w.H * w.B + t_rows * (w.B * w.H * w.N / self.cur_rows)) * 1e3
+        est = (t_rope * w.H * w.B + t_rows * (w.B * w.H * w.N / self.rows_n)) * 1e3
         return est, t_rope + t_rows
 
     def sample_text(self):
         w = self.w
-        return (f"head 0 of {w.H}: RoPE of q,k over all {w.N} tokens + {self.cur_rows} query "
+        return (f"head 0 of {w.H}: RoPE of q,k over all {w.N} tokens + {self.rows_n} query "
                 f"rows (computed pairs + merge of all {w.P} states) of the reuse step; "
-                f"extrapolated x{w.H * w.B} (RoPE) and x{w.B * w.H * w.N / self.cur_rows:.0f} (rows)")
+                f"extrapolated x{w.H * w.B} (RoPE) and x{w.B * w.H * w.N / self.rows_n:.0f} (rows)")
+
+
+def cpu_baseline(w, steps):
+    """The oracle's extrapolated step time: median over `steps` timed sample steps."""
+    base = OracleBaseline(w)
+    vals, spent = [], 0.0
+    for _ in range(steps):
+        est, sec = base.estimate_ms()
+        vals.append(est)
+        spent += sec
+    return base, statistics.median(vals), spent
 
 
 def run_reference(args, w, world=1):
-    """The oracle's time for the whole job's step: with `world` ranks that is `world` replicas
-    of the layer step (each rank of our arm runs one), all on the same host cores, so one
-    replica's extrapolated time is multiplied by `world`."""
+    """The oracle's time for one step of the whole layer, W untimed and K timed sample steps
+    (median). With `world` ranks our arm splits that same layer's heads over the ranks, so the
+    job is still one layer step; rank 0 alone runs this."""
     import numpy as np
 
     from attention_state_reuse_gb300 import workloads as wl
 
-    per_step = max(0.1, 120.0 / max(1, args.steps + args.warmup))
-    base = OracleBaseline(w, per_step)
+    base = OracleBaseline(w)
     vals = []
     for s in range(args.warmup + args.steps):
         est_ms, _ = base.estimate_ms()
         if s >= args.warmup:
             vals.append(est_ms)
-    ms = statistics.median(vals) * world
-    mask = wl.step_mask(w, 1)
-    flops = world * pair_flops(w, mask)
-    sample = base.sample_text()
-    if world > 1:
-        sample += f"; x{world} replicas (one per rank of the GPU arm) on the same cores"
+    ms = statistics.median(vals)
+    flops = pair_flops(w, wl.step_mask(w, 1))
     return {
         "metric": METRIC, "value": round(ms, 2), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "scaling": "strong", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": w.name, "B": w.B, "N": w.N, "H": w.H, "d": w.d, "P": w.P,
-                   "reuse_fraction": round(float(np.asarray(mask).mean()), 4)},
+        "config": config_of(w, world),
         "effective_tflops": round(flops / (ms * 1e-3) / 1e12, 6),
         "cpu_baseline": {"value": round(ms, 2), "unit": "ms", "cores": base.nthreads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": base.sample_text()},
         "e2e": {"value": round(ms, 2), "unit": "ms", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -574,15 +683,17 @@ def run_reference(args, w, world=1):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="wan14b_layer")
-    ap.add_argument("--cpu-budget", type=float, default=20.0,
-                    help="seconds of host CPU work for the oracle baseline sample")
+    ap.add_argument("--workload", default="long_720p")
+    ap.add_argument("--cpu-steps", type=int, default=3,
+                    help="timed oracle sample steps of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the reuse-fraction sweep")
+    ap.add_argument("--no-offload", dest="offload", action="store_false",
+                    help="skip the schedule cycle with the far pairs' states in host memory")
     ap.add_argument("--no-group", dest="group", action="store_false",
                     help="merge every reused state each step instead of one group state per row")
     ap.add_argument("--heads", type=int, default=None,
@@ -608,12 +719,10 @@ def main():
 
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-        w = replica_workload(w, rank)
     line = run_ours(args, w, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            base = OracleBaseline(w, args.cpu_budget)
-            est_ms, spent = base.estimate_ms()
+            base, est_ms, spent = cpu_baseline(w, args.cpu_steps)
             line["cpu_baseline"] = {"value": round(est_ms, 1), "unit": "ms",
                                     "cores": base.nthreads, "kind": "oracle",
                                     "sample": base.sample_text(),

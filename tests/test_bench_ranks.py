@@ -1,8 +1,12 @@
 """bench.py's multi-rank plumbing on CPU: two gloo ranks, no GPU.
 
-Under torchrun every rank runs its own replica of the layer (weak scaling, no data-path
-collective); the only cross-rank operations are the barriers around the timed region and the
-max over ranks of the measured times. These tests run that plumbing with world size 2 over gloo.
+Under torchrun the ranks split one layer's heads (every (b, h) of the method is independent:
+DiTango page, Methodology 2, Group State Computation, of which this is the single-node
+analogue): rank r computes heads [r H / N, (r + 1) H / N) with no data-path collective; the only
+cross-rank operations are the barriers around the timed region and the max over ranks of the
+measured times. These tests run that plumbing with world size 2 over gloo, check that the head
+ranges tile [0, H), and that per-rank oracle runs on their head ranges reassemble the whole
+layer's oracle result bit for bit.
 """
 import os
 import socket
@@ -63,19 +67,88 @@ def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(4.25, 1) == 4.25
 
 
-def test_replicas_have_own_inputs_and_same_shapes():
+@pytest.mark.parametrize("H", [1, 2, 7, 40])
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8])
+def test_head_ranges_tile_the_layer(H, world):
     import bench
+
+    if world > H:
+        pytest.skip("more ranks than heads")
+    ranges = [bench.head_range(r, world, H) for r in range(world)]
+    assert ranges[0][0] == 0 and ranges[-1][1] == H
+    for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+        assert a1 == b0
+    sizes = [b - a for a, b in ranges]
+    assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+
+
+def _shard_main(rank, world, port, queue):
+    # each rank runs the oracle over its own heads of one small layer with RoPE and a reuse
+    # step, then rank 0 gathers the shards
+    import torch
+    import torch.distributed as dist
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        import oracle
+        from attention_state_reuse_gb300 import workloads as wl
+
+        w = wl.scaled(wl.get("wan14b_layer"), "shard", H=5, T=2, Hl=4, Wl=6, P=4, start_frame=3)
+        h0, h1 = bench.head_range(rank, world, w.H)
+        dtt, dhh, dww = w.rope_dims
+        stream = wl.InputStream(w)
+        orc = oracle.OracleRun(w.B, w.N, h1 - h0, w.d, w.P, w.scale, nthreads=1,
+                               rope=dict(Hl=w.Hl, Wl=w.Wl, start_frame=w.start_frame, dt=dtt,
+                                         dh=dhh, dw=dww))
+        outs = []
+        for t in range(2):
+            q, k, v = (a[:, :, h0:h1] for a in stream.next())
+            res = orc.step(q, k, v, wl.step_mask(w, t))
+            # rows are (b, h_local, r) in order: back to [B, H_r, N, d]
+            outs.append(torch.from_numpy(res["out"].reshape(w.B, h1 - h0, w.N, w.d)))
+            outs.append(torch.from_numpy(res["out_lse"].reshape(w.B, h1 - h0, w.N)))
+        gathered = [None] * world if rank == 0 else None
+        dist.gather_object(outs, gathered, dst=0)
+        if rank == 0:
+            queue.put([[x.numpy() for x in g] for g in gathered])
+    finally:
+        dist.destroy_process_group()
+
+
+def test_head_shards_reassemble_the_layer_bit_for_bit():
+    import torch.multiprocessing as mp
+
+    import oracle
     from attention_state_reuse_gb300 import workloads as wl
 
-    w = wl.scaled(wl.get("wan14b_layer"), "tiny_replica", H=2, T=1, Hl=4, Wl=8)
-    r0, r1 = bench.replica_workload(w, 0), bench.replica_workload(w, 1)
-    assert (r0.N, r0.H, r0.d, r0.P) == (r1.N, r1.H, r1.d, r1.P) == (w.N, w.H, w.d, w.P)
-    a0 = wl.InputStream(r0).next()
-    a1 = wl.InputStream(r1).next()
-    for x, y in zip(a0, a1):
-        assert x.shape == y.shape
-        assert not np.array_equal(x, y)
-    assert w.index == r0.index  # the caller's workload is left alone
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_main, args=(r, 2, port, queue)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        shards = queue.get(timeout=300)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+    assert all(p.exitcode == 0 for p in procs)
+    w = wl.scaled(wl.get("wan14b_layer"), "shard", H=5, T=2, Hl=4, Wl=6, P=4, start_frame=3)
+    dtt, dhh, dww = w.rope_dims
+    full = oracle.OracleRun(w.B, w.N, w.H, w.d, w.P, w.scale, nthreads=3,
+                            rope=dict(Hl=w.Hl, Wl=w.Wl, start_frame=w.start_frame, dt=dtt,
+                                      dh=dhh, dw=dww))
+    stream = wl.InputStream(w)
+    for t in range(2):
+        res = full.step(*stream.next(), wl.step_mask(w, t))
+        out = res["out"].reshape(w.B, w.H, w.N, w.d)
+        lse = res["out_lse"].reshape(w.B, w.H, w.N)
+        got_out = np.concatenate([sh[2 * t] for sh in shards], axis=1)
+        got_lse = np.concatenate([sh[2 * t + 1] for sh in shards], axis=1)
+        assert np.array_equal(got_out, out) and np.array_equal(got_lse, lse)
 
 
 def test_algorithmic_work_accounting():
@@ -101,8 +174,9 @@ def test_algorithmic_work_accounting():
     assert bench.merge_bytes(w, zero, True) == bench.merge_bytes(w, zero, False)
 
 
-def test_reference_arm_counts_every_rank_replica(monkeypatch):
-    # the oracle does the whole job's work: one replica per rank of the GPU arm, same host cores
+def test_reference_arm_is_one_layer_step_for_any_rank_count(monkeypatch):
+    # our arm splits one layer's heads over the ranks, so the oracle's job is one layer step
+    # whatever the rank count; its config is the one our arm prints
     import argparse
 
     import bench
@@ -111,7 +185,7 @@ def test_reference_arm_counts_every_rank_replica(monkeypatch):
     class FixedOracle:
         nthreads = 4
 
-        def __init__(self, w, budget):
+        def __init__(self, w):
             pass
 
         def estimate_ms(self):
@@ -122,12 +196,14 @@ def test_reference_arm_counts_every_rank_replica(monkeypatch):
 
     monkeypatch.setattr(bench, "OracleBaseline", FixedOracle)
     args = argparse.Namespace(steps=3, warmup=3)
-    w = wl.get("wan14b_layer")
+    w = wl.get("long_720p")
     one = bench.run_reference(args, w)
     four = bench.run_reference(args, w, world=4)
-    assert one["value"] == 1000.0 and one["n_gpus"] == 1
-    assert four["value"] == 4000.0 and four["n_gpus"] == 4
-    assert four["effective_tflops"] == pytest.approx(one["effective_tflops"], rel=1e-6)
+    assert one["value"] == four["value"] == 1000.0
+    assert one["n_gpus"] == 1 and four["n_gpus"] == 4
+    assert one["config"] == bench.config_of(w, 1) and four["config"] == bench.config_of(w, 4)
+    assert one["config"]["workload"] == "long_720p" and one["config"]["reuse_mask"] == "|i-j|>=3"
     for line in (one, four):
         assert line["impl"] == "reference" and line["higher_is_better"] is False
+        assert line["scaling"] == "strong"
         assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]
