@@ -304,18 +304,17 @@ __device__ __noinline__ void rotate_q_row(uint32_t row_addr, uint32_t row_xor, i
   }
 }
 
-// P = 2^(s * scale_log2 - m) for one row of a 128-key tile, packed to bf16 pairs in pk;
-// returns the row sum of the fp32 values. Paired fp32 FMA/add instructions halve the ALU issue
-// of the scale-subtract and of the sum (four independent pair sums); the exponentials go to the
-// SFU.
-__device__ __forceinline__ float exp_pack_p(const float (&s)[kTileRows], float sl2, float m,
-                                            uint32_t (&pk)[kTileRows / 2]) {
+// P = 2^(s * scale_log2 - m) for one half row (64 keys) of a 128-key tile, packed to bf16 pairs
+// in pk (32 words); returns the sum of the fp32 values. Paired fp32 FMA/add instructions halve
+// the ALU issue of the scale-subtract and of the sum; the exponentials go to the SFU.
+__device__ __forceinline__ float exp_pack_half(const float (&s)[kTileRows / 2], float sl2, float m,
+                                               uint32_t* pk) {
   const float2 sl2x2 = make_float2(sl2, sl2);
   const float2 negm2 = make_float2(-m, -m);
   float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                   make_float2(0.f, 0.f)};
 #pragma unroll
-  for (int c = 0; c < kTileRows / 2; ++c) {
+  for (int c = 0; c < kTileRows / 4; ++c) {
     const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, negm2);
     const float p0 = ex2_approx(x.x);
     const float p1 = ex2_approx(x.y);
@@ -326,29 +325,56 @@ __device__ __forceinline__ float exp_pack_p(const float (&s)[kTileRows], float s
   return l2.x + l2.y;
 }
 
-// Row max of a tile: eight independent three-input max chains, then a short tree.
-__device__ __forceinline__ float tile_max(const float (&s)[kTileRows]) {
+// Max of a half row: eight independent three-input max chains, then a short tree.
+__device__ __forceinline__ float half_max(const float (&s)[kTileRows / 2]) {
   float m8[8];
 #pragma unroll
   for (int x = 0; x < 8; ++x) m8[x] = fmaxf(s[x], s[8 + x]);
 #pragma unroll
-  for (int c = 16; c < kTileRows; c += 16)
+  for (int c = 16; c < kTileRows / 2; c += 16)
 #pragma unroll
     for (int x = 0; x < 8; ++x) m8[x] = fmax3(m8[x], s[c + x], s[c + 8 + x]);
   return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
-// Reads S (one row of 128 fp32 scores per thread) from TMEM; keys at or past `valid` get -inf.
-__device__ __forceinline__ void load_s(uint32_t s_taddr, int valid, float (&s)[kTileRows]) {
-  uint32_t r[kTileRows];
-  tmem_ld_32x32b_x128(s_taddr, r);
+// Reads half h of a row of S (64 fp32 scores per thread) from TMEM; keys at or past `valid`
+// (counted from the start of the tile) get -inf.
+__device__ __forceinline__ void load_s_half(uint32_t s_taddr, int h, int valid,
+                                            float (&s)[kTileRows / 2]) {
+  uint32_t r[kTileRows / 2];
+  tmem_ld_32x32b_x64(s_taddr + h * (kTileRows / 2), r);
 #pragma unroll
-  for (int c = 0; c < kTileRows; ++c) s[c] = __uint_as_float(r[c]);
-  if (valid < kTileRows) {
+  for (int c = 0; c < kTileRows / 2; ++c) s[c] = __uint_as_float(r[c]);
+  const int v = valid - h * (kTileRows / 2);
+  if (v < kTileRows / 2) {
 #pragma unroll
-    for (int c = 0; c < kTileRows; ++c)
-      if (c >= valid) s[c] = -INFINITY;
+    for (int c = 0; c < kTileRows / 2; ++c)
+      if (c >= v) s[c] = -INFINITY;
   }
+}
+
+// Exact row max of a tile (both halves).
+__device__ __forceinline__ float row_max(uint32_t s_taddr, int valid) {
+  float s[kTileRows / 2];
+  load_s_half(s_taddr, 0, valid, s);
+  const float m0 = half_max(s);
+  load_s_half(s_taddr, 1, valid, s);
+  return fmaxf(m0, half_max(s));
+}
+
+// P of a whole tile row into pk (64 words), half by half: 64 scores live at a time instead of
+// 128 keep the softmax within its 168 registers (the whole-row form spilled; measured 2-4%
+// slower); returns the row sum.
+__device__ __forceinline__ float exp_pack_row(uint32_t s_taddr, int valid, float sl2, float m,
+                                              uint32_t (&pk)[kTileRows / 2]) {
+  float l = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float s[kTileRows / 2];
+    load_s_half(s_taddr, h, valid, s);
+    l += exp_pack_half(s, sl2, m, pk + h * (kTileRows / 4));
+  }
+  return l;
 }
 
 template <int D>
@@ -553,17 +579,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after_sync();
           const int valid = nj - t * kTileRows;
-          float s[kTileRows];
-          load_s(s_taddr, valid, s);
-          if (t == 0) m_run = tile_max(s) * sl2;  // first tile of the partition: exact max
+          if (t == 0) m_run = row_max(s_taddr, valid) * sl2;  // first tile: exact max
           uint32_t pk[kTileRows / 2];
-          float l_t = exp_pack_p(s, sl2, m_run, pk);
+          float l_t = exp_pack_row(s_taddr, valid, sl2, m_run, pk);
           const bool redo = t > 0 && !(l_t <= kRescaleSum);
           if (__any_sync(0xffffffffu, redo)) {
             // the rows whose sum left the range move m to the exact max of this tile (S is
             // re-read: it is still intact in TMEM), rescale O and l, and recompute P
-            load_s(s_taddr, valid, s);
-            const float m_tile = tile_max(s) * sl2;
+            const float m_tile = row_max(s_taddr, valid) * sl2;
             float alpha = 1.f;
             if (redo) {
               const float m_new = fmaxf(m_run, m_tile);
@@ -583,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
               tmem_st_32x32b_x32(o_taddr + c * 32, r);
             }
-            l_t = exp_pack_p(s, sl2, m_run, pk);
+            l_t = exp_pack_row(s_taddr, valid, sl2, m_run, pk);
           }
           {
             uint32_t lo[32], hi[32];

@@ -577,7 +577,7 @@ def max_over_ranks(x, world):
 
 
 # ------------------------------------------------------------------------------ CPU oracle
-SAMPLE_ROWS = 2048  # query rows of head 0 the oracle computes per timed step
+SAMPLE_ROWS = 12288  # query rows of head 0 the oracle computes per timed step
 
 
 class OracleBaseline:
