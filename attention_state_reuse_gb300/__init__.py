@@ -519,13 +519,13 @@ class AnchorPlanner:
     """Drives the reuse masks of one layer: every `anchor_every` steps an anchor step computes
     every pair, after which the importance weights are refreshed and the local states are
     snapshotted; on the other steps the drift since the anchor and the weights choose the mask
-    (planner_select with tau, group and budget)."""
+    (planner_select with tau, group and budget). `host`: the cache's host storage, if any."""
 
     def __init__(self, plan: Plan, cache_O, cache_lse, anchor_every: int, tau: float,
-                 group: int = 1, budget: int = -1):
+                 group: int = 1, budget: int = -1, host=None):
         import torch
 
-        self.plan, self.cO, self.cL = plan, cache_O, cache_lse
+        self.plan, self.cO, self.cL, self.host = plan, cache_O, cache_lse, host
         self.anchor_every, self.tau, self.group, self.budget = anchor_every, tau, group, budget
         B, H, P, N, d = cache_O.shape
         self.snapshot = torch.empty((B, H, N, d), dtype=cache_O.dtype, device=cache_O.device)
@@ -538,7 +538,8 @@ class AnchorPlanner:
 
         if self.w is None or self.t % self.anchor_every == 0:
             return np.zeros((self.plan.P, self.plan.P), np.uint8)
-        delta = planner_drift(self.plan, self.cO, self.cL, self.snapshot).cpu().numpy()
+        delta = planner_drift(self.plan, self.cO, self.cL, self.snapshot,
+                              host=self.host).cpu().numpy()
         return planner_select(self.plan, self.w, delta, self.tau, self.group, self.budget)
 
     def after_step(self, mask) -> None:
@@ -546,8 +547,8 @@ class AnchorPlanner:
         import numpy as np
 
         if not np.asarray(mask).any():
-            self.w = planner_importance(self.plan, self.cO, self.cL).cpu().numpy()
-            planner_snapshot(self.plan, self.cO, self.cL, self.snapshot)
+            self.w = planner_importance(self.plan, self.cO, self.cL, host=self.host).cpu().numpy()
+            planner_snapshot(self.plan, self.cO, self.cL, self.snapshot, host=self.host)
         self.t += 1
 
 

@@ -180,3 +180,25 @@ def test_host_storage_errors():
                                ctypes.c_size_t(0), None)
     assert dt.STATUS[st] == "SHAPE"
     assert lay.plan.cache_state()[2] == 0
+
+
+def test_anchor_planner_drives_an_offloaded_cache():
+    # the planner's reductions read the host-resident states through the slot map; its masks
+    # drive steps whose outputs match the oracle
+    w = wl.scaled(wl.get("small_bf16"), "offload_anchor", H=2, steps=6)
+    lay = Layer(w, 3)
+    planner = dt.AnchorPlanner(lay.plan, lay.cO, lay.cL, anchor_every=3, tau=0.0, group=2,
+                               budget=w.P + 8, host=lay.host)
+    orc = oracle.OracleRun(w.B, w.N, w.H, w.d, w.P, w.scale)
+    stream = wl.InputStream(w)
+    for t in range(6):
+        q, k, v = stream.next()
+        mask = planner.mask()
+        assert mask.shape == (w.P, w.P) and (np.diag(mask) == 0).all()
+        lay.step(*(torch.from_numpy(a).cuda().to(torch.bfloat16) for a in (q, k, v)), mask)
+        planner.after_step(mask)
+        torch.cuda.synchronize()
+        ref = orc.step(q, k, v, mask)
+        got = lay.out.float().cpu().numpy().transpose(0, 2, 1, 3).reshape(-1, w.d)
+        assert np.abs(got - ref["out"]).max() <= 2e-2
+        assert np.abs(lay.out_lse.cpu().numpy().reshape(-1) - ref["out_lse"]).max() <= 1e-3
