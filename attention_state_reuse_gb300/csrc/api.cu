@@ -421,12 +421,24 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   // its partition's reused pairs (built in the same pass where it is missing or out of date)
   if (!mark(2)) return DITANGO_ERR_CUDA;
   uint64_t reused[kMaxP] = {}, rebuild = 0;
+  bool any_reuse = false;
   for (int32_t i = 0; i < P; ++i) {
     reused[i] = plan_reused_set(plan, reuse_mask, i);
+    any_reuse |= reused[i] != 0;
     if (use_group && reused[i] != 0 && !plan_group_current(plan, gO.ptr, i, reused[i]))
       rebuild |= uint64_t{1} << i;
   }
-  for (uint64_t m = rebuild; m; m &= m - 1)
+  // A step that computes every pair, on a plan whose default mask reuses some: the merge, which
+  // reads every state anyway, also builds the group states of the default mask's reused sets
+  // from this step's states, so that the next step under that mask finds them current.
+  uint64_t ahead = 0, ahead_set[kMaxP] = {};
+  if (use_group && !any_reuse && reuse_mask != nullptr) {
+    for (int32_t i = 0; i < P; ++i) {
+      ahead_set[i] = plan_reused_set(plan, nullptr, i);
+      if (ahead_set[i] != 0) ahead |= uint64_t{1} << i;
+    }
+  }
+  for (uint64_t m = rebuild | ahead; m; m &= m - 1)
     plan->group_set[__builtin_ctzll(m)] = 0;  // invalid until this build has been launched
   StepMergeArgs ma;
   std::memset(&ma, 0, sizeof(ma));
@@ -437,12 +449,13 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
   for (int32_t i = 0; i <= P; ++i) ma.offsets[i] = static_cast<int32_t>(plan->offsets[i]);
   for (int32_t i = 0; i < P; ++i) {
     const uint64_t all = P == 64 ? ~uint64_t{0} : (uint64_t{1} << P) - 1;
-    const bool grp = use_group && reused[i] != 0;
-    ma.cache_set[i] = grp ? (all & ~reused[i]) : all;
-    ma.reused_set[i] = reused[i];
+    const uint64_t set = (ahead >> i) & 1u ? ahead_set[i] : reused[i];
+    const bool grp = use_group && set != 0;
+    ma.cache_set[i] = grp ? (all & ~set) : all;
+    ma.reused_set[i] = set;
     if (grp) ma.group |= uint64_t{1} << i;
   }
-  ma.rebuild = rebuild;
+  ma.rebuild = rebuild | ahead;
   ma.cache = loc;
   ma.gO = use_group ? static_cast<float*>(gO.ptr) : nullptr;
   ma.gL = use_group ? static_cast<float*>(gL.ptr) : nullptr;
@@ -460,6 +473,11 @@ int ditango_attn_step(ditango_plan_t plan, const ditango_tensor* q, const ditang
     plan_group_built(plan, gO.ptr, i, reused[i]);
   }
   plan_commit(plan, reuse_mask);
+  // the groups built ahead hold states computed at this step: recorded after the commit
+  for (uint64_t m = ahead; m; m &= m - 1) {
+    const int32_t i = __builtin_ctzll(m);
+    plan_group_built(plan, gO.ptr, i, ahead_set[i]);
+  }
   return DITANGO_OK;
 }
 

@@ -219,7 +219,10 @@ def run_ours(args, w, rank, world):
     q_np, k_np, v_np = (np.ascontiguousarray(a[:, :, h0:h1]) for a in stream.next())
     to_dev = lambda a: torch.from_numpy(a).to(dev).to(dtype)
     q, k, v = to_dev(q_np), to_dev(k_np), to_dev(v_np)
-    plan = dt.Plan(N, P)
+    mask = wl.step_mask(w, 1)  # the steady-state reuse step of the workload's schedule
+    # the plan's default mask is the steady reuse mask: the anchor's merge then builds the
+    # group states that the reuse steps after it read
+    plan = dt.Plan(N, P, mask=mask)
     cO, cL = dt.new_state_cache(B, H, P, N, d, dtype, dev)
     out = torch.empty((B, N, H, d), dtype=dtype, device=dev)
     out_lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -232,7 +235,6 @@ def run_ours(args, w, rank, world):
                      device=dev)
     group = dt.new_group_state(B, H, N, d, dev) if args.group else None
     anchor = np.zeros((P, P), np.uint8)
-    mask = wl.step_mask(w, 1)  # the steady-state reuse step of the workload's schedule
     step = lambda m: dt.attn_step(plan, q, k, v, cO, cL, out, out_lse, reuse_mask=m, rope=rope,
                                   softmax_scale=w.scale, workspace=ws, group=group)
 
@@ -247,8 +249,8 @@ def run_ours(args, w, rank, world):
         ev[1].record()
         torch.cuda.synchronize()
         anchor_ms.append(ev[0].elapsed_time(ev[1]))
-    # the first reuse step after the anchor also builds the group states (once per change of
-    # the reused sets); it is timed on its own, the steady-state steps below reuse them
+    # the first reuse step after an anchor, timed on its own: it finds the group states that
+    # the anchor built current, so it costs what a steady-state step costs
     ev[0].record()
     step(mask)
     ev[1].record()
@@ -455,6 +457,7 @@ def offload_cycle(w, q, k, v, dev, cycles=2):
     ws = torch.empty(max(1, dt.workspace_size(plan, B, H, d, dtype, w.rope)), dtype=torch.uint8,
                      device=dev)
     sched = [wl.step_mask(w, t) for t in range(len(w.schedule))]
+    plan.set_mask(sched[1])  # the anchors build the reuse steps' group states
     period = next((t for t in range(1, len(sched)) if not sched[t].any()), len(sched))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(period + 1)]
     times = []

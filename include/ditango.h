@@ -97,9 +97,15 @@ typedef struct {
  * recomputation, and the result is itself a state). When present, a step merges every row's
  * computed states with the single group state of its partition's reused pairs instead of with
  * each reused state. The library builds a partition's group state (one merge of its reused
- * cached states) at a step whose reused set differs from the one the group was built from, or
- * when one of those pairs has been recomputed since; the plan records this, so pass the same
- * buffers with the same plan every step (other buffers make it rebuild). */
+ * cached states, in the step's merge pass) at a step whose reused set differs from the one the
+ * group was built from, or when one of those pairs has been recomputed since; the plan records
+ * this, so pass the same buffers with the same plan every step (other buffers make it rebuild).
+ * A step that computes every pair (reuse_mask given, all zero) on a plan whose default mask
+ * (ditango_plan / ditango_plan_set_mask) reuses pairs builds, in its merge pass, the group
+ * states of that default mask's reused sets from its own fresh states: a following step under
+ * the default mask then finds them current (DiTango, Methodology 2, Pipeline Orchestration:
+ * the reuse work rides on a pass that runs anyway). Its output is the same merge of all states,
+ * taken through the group state. */
 typedef struct {
   ditango_tensor O;
   ditango_tensor lse;

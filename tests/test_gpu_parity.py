@@ -81,6 +81,37 @@ def test_group_state_buffer_swap_rebuilds():
     assert pr.step(mask=wl.distance_mask(w.P, 2))["ok"]
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_group_built_ahead_at_all_compute_step(dtype):
+    # a plan whose default mask reuses |i - j| >= 2: the step that computes every pair builds
+    # those group states from its own states, so the reuse steps after it read no cached state
+    # of a reused pair (poisoned here with NaN) and give the outputs, bit for bit, of a plan
+    # that builds the same group states at the first reuse step
+    base = wl.get("small_bf16") if dtype == "bf16" else wl.get("tiny_fp32")
+    w = wl.scaled(base, f"ahead_{dtype}", H=2, steps=4)
+    P = w.P
+    D2, ALL = wl.distance_mask(P, 2), np.zeros((P, P), np.uint8)
+    ahead, lazy = ParityRun(w, group=True), ParityRun(w, group=True)
+    ahead.plan.set_mask(D2)
+    for pr in (ahead, lazy):
+        assert pr.step(mask=ALL)["ok"]
+    off = ahead.plan.offsets()
+    built = torch.isfinite(ahead.group[1]).all().item()
+    assert built, "the all-compute step left group states unbuilt"
+    assert torch.isnan(lazy.group[1]).all().item()
+    for i in range(P):
+        for j in np.nonzero(D2[i])[0]:
+            ahead.cO[:, :, j, off[i]:off[i + 1]] = float("nan")
+            ahead.cL[:, :, j, off[i]:off[i + 1]] = float("nan")
+    for _ in range(2):
+        ahead.step(mask=D2, check=False)
+        assert lazy.step(mask=D2)["ok"]
+        assert torch.equal(ahead.out, lazy.out)
+        assert torch.equal(ahead.out_lse, lazy.out_lse)
+        assert torch.equal(ahead.group[0], lazy.group[0])
+        assert torch.equal(ahead.group[1], lazy.group[1])
+
+
 def test_rope_d64_even_table_halves():
     # d = 64: 12/10/10 channel pairs per axis (even halves, padded to odd strides in the
     # shared-memory table), 4 frames from global frame 3, Q tiles spanning frame boundaries
