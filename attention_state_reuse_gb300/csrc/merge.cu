@@ -10,8 +10,8 @@
 //
 // Thread layout: grid.y walks the row groups (a (b, h) slab; launched in chunks of at most
 // 65535), grid.x the rows of a group; each row is handled by d/VEC consecutive threads, each
-// owning VEC contiguous channels loaded as one 16-byte vector per state, so a warp reads whole
-// rows of every state in fully used 32-byte sectors. Index arithmetic is 32-bit (shifts and
+// owning VEC contiguous channels loaded as VPT 16-byte vectors per state (one for a state list,
+// two for a step), so a warp reads whole rows of every state in fully used 32-byte sectors. Index arithmetic is 32-bit (shifts and
 // masks when d/VEC is a power of two, a division otherwise); exponentials and the logarithm use
 // the SFU approximations (relative error ~2^-22). States are merged online in rounds whose
 // vectors and lse values are all loaded before any is used, so a round costs one memory round
@@ -40,17 +40,26 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void store_vec(float* p, const float (&x)[4]) {
-  *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-}
-__device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&x)[8]) {
-  uint32_t w[4];
+// VEC fp32 channels (VEC / 4 vectors of 16 bytes).
+template <int VEC>
+__device__ __forceinline__ void store_vec(float* p, const float (&x)[VEC]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  for (int q = 0; q < VEC / 4; ++q)
+    reinterpret_cast<float4*>(p)[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+}
+// VEC bf16 channels (VEC / 8 vectors of 16 bytes), each rounded to nearest even.
+template <int VEC>
+__device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&x)[VEC]) {
+#pragma unroll
+  for (int q = 0; q < VEC / 8; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(x[8 * q + 2 * i], x[8 * q + 2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(p)[q] = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 // VEC fp32 channels, 16-byte aligned (group states are fp32 whatever the cache dtype).
 template <int VEC>
@@ -102,12 +111,12 @@ struct RowStates {
 };
 
 // Loads the next round of up to NS states of `m` (a bit set of states j, lowest first): the
-// 16-byte vector of this thread's channels and the lse (log2 units) of each, all issued before
-// any is used, so that a round costs one memory round trip. Slots past the set get lse = -inf
-// and a zero vector. Returns how many states were loaded; m loses their bits.
-template <typename T, int NS>
-__device__ __forceinline__ int load_round(uint64_t& m, const RowStates& rs, uint4 (&raw)[NS],
-                                          float (&l)[NS]) {
+// VPT 16-byte vectors of this thread's channels and the lse (log2 units) of each, all issued
+// before any is used, so that a round costs one memory round trip. Slots past the set get
+// lse = -inf and zero vectors. Returns how many states were loaded; m loses their bits.
+template <typename T, int NS, int VPT>
+__device__ __forceinline__ int load_round(uint64_t& m, const RowStates& rs,
+                                          uint4 (&raw)[NS][VPT], float (&l)[NS]) {
   int cnt = 0;
 #pragma unroll
   for (int q = 0; q < NS; ++q) {
@@ -117,11 +126,13 @@ __device__ __forceinline__ int load_round(uint64_t& m, const RowStates& rs, uint
       const T* o;
       const float* lp;
       rs.ptrs<T>(j, o, lp);
-      raw[q] = load_raw(o);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) raw[q][v] = load_raw(o + v * (16 / sizeof(T)));
       l[q] = __ldg(lp) * kLog2e;
       ++cnt;
     } else {
-      raw[q] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) raw[q][v] = make_uint4(0u, 0u, 0u, 0u);
       l[q] = -INFINITY;
     }
   }
@@ -130,9 +141,10 @@ __device__ __forceinline__ int load_round(uint64_t& m, const RowStates& rs, uint
 
 // Online merge of one loaded round into (mx, sum, acc), all relative to the running max mx
 // (log2 units): acc and sum are rescaled by 2^(mx - mx_new) once per round.
-template <typename T, int VEC, int NS>
-__device__ __forceinline__ void merge_round(const uint4 (&raw)[NS], const float (&l)[NS], int cnt,
-                                            float& mx, float& sum, float (&acc)[VEC]) {
+template <typename T, int VEC, int NS, int VPT>
+__device__ __forceinline__ void merge_round(const uint4 (&raw)[NS][VPT], const float (&l)[NS],
+                                            int cnt, float& mx, float& sum, float (&acc)[VEC]) {
+  constexpr int H = VEC / VPT;  // channels per vector
   float mn = mx;
 #pragma unroll
   for (int q = 0; q < NS; ++q) mn = fmaxf(mn, l[q]);
@@ -145,24 +157,27 @@ __device__ __forceinline__ void merge_round(const uint4 (&raw)[NS], const float 
     if (q < cnt) {
       const float w = ex2(l[q] - mn);
       sum += w;
-      float x[VEC];
-      unpack(raw[q], x, static_cast<const T*>(nullptr));
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+      for (int v = 0; v < VPT; ++v) {
+        float x[H];
+        unpack(raw[q][v], x, static_cast<const T*>(nullptr));
+#pragma unroll
+        for (int e = 0; e < H; ++e) acc[v * H + e] = fmaf(w, x[e], acc[v * H + e]);
+      }
     }
   }
   mx = mn;
 }
 
 // Merges every state of the bit set `set` (states j of this row) into (mx, sum, acc).
-template <typename T, int VEC, int NS>
+template <typename T, int VEC, int NS, int VPT>
 __device__ __forceinline__ void merge_set(uint64_t set, const RowStates& rs, float& mx, float& sum,
                                           float (&acc)[VEC]) {
   for (uint64_t m = set; m != 0;) {
-    uint4 raw[NS];
+    uint4 raw[NS][VPT];
     float l[NS];
-    const int cnt = load_round<T, NS>(m, rs, raw, l);
-    merge_round<T, VEC, NS>(raw, l, cnt, mx, sum, acc);
+    const int cnt = load_round<T, NS, VPT>(m, rs, raw, l);
+    merge_round<T, VEC, NS, VPT>(raw, l, cnt, mx, sum, acc);
   }
 }
 
@@ -206,20 +221,20 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   for (int s0 = 0; s0 < a.n; s0 += NS) {
-    uint4 raw[NS];
+    uint4 raw[NS][1];
     float l[NS];
     const int cnt = min(NS, a.n - s0);
 #pragma unroll
     for (int q = 0; q < NS; ++q) {
       if (q < cnt) {
-        raw[q] = load_raw(static_cast<const T*>(a.O[s0 + q]) + oo);
+        raw[q][0] = load_raw(static_cast<const T*>(a.O[s0 + q]) + oo);
         l[q] = __ldg(a.lse[s0 + q] + lo) * kLog2e;
       } else {
-        raw[q] = make_uint4(0u, 0u, 0u, 0u);
+        raw[q][0] = make_uint4(0u, 0u, 0u, 0u);
         l[q] = -INFINITY;
       }
     }
-    merge_round<T, VEC, NS>(raw, l, cnt, mx, sum, acc);
+    merge_round<T, VEC, NS, 1>(raw, l, cnt, mx, sum, acc);
   }
   const float lse = (mx + lg2(sum)) * kLn2;
   const float inv = 1.f / sum;
@@ -243,17 +258,22 @@ __global__ void __launch_bounds__(kMergeThreads)
 // host slot (CacheLoc).
 // Starting from a group state built here or loaded gives the same arithmetic (the same fp32
 // values), so a rebuild step and a steady step agree bit for bit on the same states.
-// NS: states per round (each round's loads are issued together).
-// At most 40 registers (six blocks of 256 threads per SM): measured 0.350 ms on the Wan-14B
-// layer's step against 0.382 ms at the compiler's 44 (five blocks); 32 (eight blocks) spills.
+// NS: states per round (each round's loads are issued together). Each thread owns two 16-byte
+// vectors of a row (VEC = 32 / sizeof(T) channels), which halves the per-state index and
+// address work per byte: measured 0.904 ms for the 720p layer's step (6.6 TB/s) against 1.086
+// ms with one vector per thread, and 0.299 against 0.349 ms on the Wan-14B layer. At most 64
+// registers (four blocks of 256 threads per SM): the cap of 48 (five blocks) spills and
+// measured 0.982 ms.
 template <typename T, int NS>
-__global__ void __launch_bounds__(kMergeThreads, 6)
+__global__ void __launch_bounds__(kMergeThreads, 4)
     step_merge_kernel(const __grid_constant__ StepMergeArgs a, int64_t bh_base) {
-  constexpr int VEC = 16 / sizeof(T);
-  constexpr int VEC_SHIFT = VEC == 8 ? 3 : 2;
+  constexpr int VPT = 2;
+  constexpr int VEC = VPT * 16 / sizeof(T);
+  constexpr int VEC_SHIFT = VEC == 16 ? 4 : 3;
+  static_assert(VEC == 1 << VEC_SHIFT, "channels per thread");
   uint32_t r;
   int c0;
-  const int tpr_shift = 31 - __clz(a.d) - VEC_SHIFT;  // d / VEC is 8 or 16 (d = 64 or 128)
+  const int tpr_shift = 31 - __clz(a.d) - VEC_SHIFT;  // d / VEC is 4, 8 or 16 (d = 64 or 128)
   const bool live = thread_row(a.N, a.d / VEC, tpr_shift, VEC_SHIFT, r, c0);
   // launched as a programmatic dependent of the pair kernel: everything below reads states it
   // wrote, so wait for that grid to complete (a no-op for an ordinary launch)
@@ -270,7 +290,7 @@ __global__ void __launch_bounds__(kMergeThreads, 6)
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   if ((a.rebuild >> i) & 1u) {
     // Dynamic Group Compose: the reused states merge into the row's group state
-    merge_set<T, VEC, NS>(a.reused_set[i], rs, mx, sum, acc);
+    merge_set<T, VEC, NS, VPT>(a.reused_set[i], rs, mx, sum, acc);
     const float g_lse = (mx + lg2(sum)) * kLn2;
     const float inv = 1.f / sum;
 #pragma unroll
@@ -284,7 +304,7 @@ __global__ void __launch_bounds__(kMergeThreads, 6)
     sum = 1.f;
     load_f32<VEC>(a.gO + (bh * a.N + r) * a.d + c0, acc);
   }
-  merge_set<T, VEC, NS>(a.cache_set[i], rs, mx, sum, acc);
+  merge_set<T, VEC, NS, VPT>(a.cache_set[i], rs, mx, sum, acc);
   const float lse = (mx + lg2(sum)) * kLn2;
   const float inv = 1.f / sum;
 #pragma unroll
@@ -332,7 +352,7 @@ cudaError_t launch_step_typed(const StepMergeArgs& a, dim3 grid, int64_t g0, cud
 }  // namespace
 
 cudaError_t launch_step_merge(const StepMergeArgs& a, cudaStream_t stream) {
-  const int vec = a.dtype == DITANGO_BF16 ? 8 : 4;
+  const int vec = a.dtype == DITANGO_BF16 ? 16 : 8;  // channels per thread (two vectors)
   const int64_t groups = a.B * a.H;
   if (groups == 0 || a.N == 0) return cudaSuccess;
   if (a.d != 64 && a.d != 128) return cudaErrorInvalidValue;
