@@ -250,9 +250,16 @@ def run_ours(args, w, rank, world):
         torch.cuda.synchronize()
         anchor_ms.append(ev[0].elapsed_time(ev[1]))
     # the first reuse step after an anchor, timed on its own: it finds the group states that
-    # the anchor built current, so it costs what a steady-state step costs
+    # the anchor built current; its kernels are timed too
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(3)]
+    for evs in fev:
+        for e in evs:
+            e.record()
+    torch.cuda.synchronize()
     ev[0].record()
+    plan.set_profile_events(fev[0])
     step(mask)
+    plan.set_profile_events(None)
     ev[1].record()
     torch.cuda.synchronize()
     first_reuse_ms = ev[0].elapsed_time(ev[1])
@@ -355,14 +362,19 @@ def run_ours(args, w, rank, world):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     # two more (anchor, first reuse step) cycles: first_reuse_step_ms is the median of three
     first_reuse = [first_reuse_ms]
-    for _ in range(2):
+    for c in range(2):
         step(anchor)
         ev[0].record()
+        plan.set_profile_events(fev[c + 1])
         step(mask)
+        plan.set_profile_events(None)
         ev[1].record()
         torch.cuda.synchronize()
         first_reuse.append(ev[0].elapsed_time(ev[1]))
     first_reuse_ms = statistics.median(first_reuse)
+    first_kernel_ms = {name: round(statistics.median(fev[c][x].elapsed_time(fev[c][x + 1])
+                                                     for c in range(3)), 4)
+                       for x, name in enumerate(("rope", "pair", "merge"))}
     esz = 2 if dtype == torch.bfloat16 else 4
     # bytes of the whole job (every rank copies its own heads)
     h2d = 3 * B * N * w.H * d * esz
@@ -401,6 +413,7 @@ def run_ours(args, w, rank, world):
                       "merge": round(merge_ms, 4)},
         "anchor_ms": round(statistics.median(anchor_ms), 4),
         "first_reuse_step_ms": round(first_reuse_ms, 4),
+        "first_reuse_kernel_ms": first_kernel_ms,
         "group_states": bool(args.group),
         "anchor_effective_tflops": round(pair_flops(w, anchor) / (statistics.median(anchor_ms) * 1e-3) / 1e12, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_burst,
