@@ -519,24 +519,34 @@ class AnchorPlanner:
     """Drives the reuse masks of one layer: every `anchor_every` steps an anchor step computes
     every pair, after which the importance weights are refreshed and the local states are
     snapshotted; on the other steps the drift since the anchor and the weights choose the mask
-    (planner_select with tau, group and budget). `host`: the cache's host storage, if any."""
+    (planner_select with tau, group and budget). `host`: the cache's host storage, if any.
+
+    build_ahead: before each anchor after the first, the plan's default mask is set to the
+    mask chosen right after the previous anchor, so that the anchor's merge builds those group
+    states (ditango_attn_step does so for an all-compute step); when the next choice is the same
+    mask, its step finds them current. The masks this class returns are always explicit."""
 
     def __init__(self, plan: Plan, cache_O, cache_lse, anchor_every: int, tau: float,
-                 group: int = 1, budget: int = -1, host=None):
+                 group: int = 1, budget: int = -1, host=None, build_ahead: bool = True):
         import torch
 
         self.plan, self.cO, self.cL, self.host = plan, cache_O, cache_lse, host
         self.anchor_every, self.tau, self.group, self.budget = anchor_every, tau, group, budget
+        self.build_ahead = build_ahead
         B, H, P, N, d = cache_O.shape
         self.snapshot = torch.empty((B, H, N, d), dtype=cache_O.dtype, device=cache_O.device)
         self.w = None
         self.t = 0
+        self._last_anchor = False  # the previous step was an anchor
+        self.predicted = None      # the mask chosen right after the last anchor
 
     def mask(self):
         """Reuse mask for the next step."""
         import numpy as np
 
         if self.w is None or self.t % self.anchor_every == 0:
+            if self.build_ahead and self.predicted is not None:
+                self.plan.set_mask(self.predicted)
             return np.zeros((self.plan.P, self.plan.P), np.uint8)
         delta = planner_drift(self.plan, self.cO, self.cL, self.snapshot,
                               host=self.host).cpu().numpy()
@@ -546,9 +556,15 @@ class AnchorPlanner:
         """Call after the step that used `mask`: an all-compute step becomes the anchor."""
         import numpy as np
 
-        if not np.asarray(mask).any():
+        m = np.asarray(mask)
+        if not m.any():
             self.w = planner_importance(self.plan, self.cO, self.cL, host=self.host).cpu().numpy()
             planner_snapshot(self.plan, self.cO, self.cL, self.snapshot, host=self.host)
+            self._last_anchor = True
+        else:
+            if self._last_anchor:
+                self.predicted = np.array(m, dtype=np.uint8, copy=True)
+            self._last_anchor = False
         self.t += 1
 
 

@@ -74,8 +74,11 @@ class Layer:
         return O, L
 
 
-def run_pair(w, S, masks, group=True):
+def run_pair(w, S, masks, group=True, default_mask=None):
     res, off = Layer(w, None, group), Layer(w, S, group)
+    if default_mask is not None:  # the anchors also build the default mask's group states
+        res.plan.set_mask(default_mask)
+        off.plan.set_mask(default_mask)
     stream = wl.InputStream(w)
     dev = torch.device("cuda")
     for t, mask in enumerate(masks):
@@ -92,14 +95,16 @@ def run_pair(w, S, masks, group=True):
     return res, off
 
 
-def test_720p_layer_schedule_with_host_storage_matches_device_cache():
+@pytest.mark.parametrize("ahead", [False, True])
+def test_720p_layer_schedule_with_host_storage_matches_device_cache(ahead):
     # the 720p-shaped layer at its stated N (75600 tokens, P = 16, RoPE) on 4 heads, over its
     # eight-step schedule (anchor, |i - j| >= 3 reused, refresh at step 4), with S = 2 * 3 - 1
     # device slots per row: the steady steps compute device-resident pairs only; the anchors
-    # write the far pairs into host memory and the group rebuilds read them back
+    # write the far pairs into host memory and the group rebuilds read them back (ahead: the
+    # plans' default mask is the reuse mask, so the anchors' merges build the group states)
     w = wl.scaled(wl.get("long_720p"), "long_offload", H=4)
     masks = [wl.step_mask(w, t) for t in range(w.steps)]
-    run_pair(w, 5, masks)
+    run_pair(w, 5, masks, default_mask=masks[1] if ahead else None)
 
 
 @pytest.mark.parametrize("dtype,S", [("bf16", 3), ("bf16", 1), ("fp32", 2)])

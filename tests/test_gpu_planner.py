@@ -125,3 +125,27 @@ def test_anchor_planner_drives_steps():
     assert all(np.all(np.diag(m) == 0) for m in between)
     assert any(m.any() for m in between)          # something was reused
     assert any((m == 0).sum() > 8 for m in between)  # and something beyond the diagonal computed
+
+
+def test_anchor_planner_builds_group_states_ahead():
+    # two planner-driven runs on the same inputs, with and without the ahead-of-time group
+    # build: the masks agree, every step matches the oracle, and the non-anchor steps agree bit
+    # for bit (a group state built at the anchor holds the same values as one built at the
+    # first reuse step, from the same cached states)
+    sched = [("all",)] * 10
+    w = wl.Workload("planned_ahead", 2, 1, 3, 64, 4, 16, 16, 8, "bf16", len(sched), 0.05,
+                    schedule=sched)
+    runs = [ParityRun(w, group=True), ParityRun(w, group=True)]
+    aps = [dt.AnchorPlanner(r.plan, r.cO, r.cL, anchor_every=4, tau=1e-3, group=2,
+                            build_ahead=b) for r, b in zip(runs, (True, False))]
+    for t in range(len(sched)):
+        ms = [ap.mask() for ap in aps]
+        assert np.array_equal(ms[0], ms[1]), t
+        for r, ap, m in zip(runs, aps, ms):
+            e = r.step(mask=m)
+            assert e["ok"], (t, e)
+            ap.after_step(m)
+        if ms[0].any():
+            assert torch.equal(runs[0].out, runs[1].out), t
+            assert torch.equal(runs[0].out_lse, runs[1].out_lse), t
+    assert aps[0].predicted is not None and aps[0].predicted.any()
