@@ -340,10 +340,10 @@ cudaError_t launch_step_chunk(const StepMergeArgs& a, dim3 grid, int64_t g0, cud
   return cudaLaunchKernelEx(&cfg, step_merge_kernel<T, NS>, a, g0);
 }
 
-// Rounds of two states: measured faster than whole-row rounds (Wan-14B layer 0.353 ms against
-// 0.432 ms with rounds of four, 720p layer 1.08 ms against 1.74 ms with rounds of eight): fewer
-// registers per thread keep more rows in flight per SM, which matters more than the loads each
-// thread issues at once.
+// Rounds of two states: measured faster than whole-row rounds (with one vector per thread,
+// Wan-14B layer 0.353 ms against 0.432 ms with rounds of four, 720p layer 1.08 ms against 1.74
+// ms with rounds of eight; with two, 0.90 ms against 1.06 ms with rounds of three and 0.92-1.01
+// ms with rounds of one): fewer registers per thread keep more rows in flight per SM.
 template <typename T>
 cudaError_t launch_step_typed(const StepMergeArgs& a, dim3 grid, int64_t g0, cudaStream_t stream) {
   return launch_step_chunk<T, 2>(a, grid, g0, stream);
