@@ -170,6 +170,9 @@ class ClockSampler:
 # dense bf16 tcgen05 rate of one SM: a 128x128x16 MMA (2^19 flops) every 64 cycles, measured
 # with MMAs issued back to back on this GPU
 DENSE_BF16_FLOP_PER_CLK_SM = 8192
+# SFU exponentials of one SM per clock (ex2.approx, fp32 and bf16x2 alike), measured with a
+# throughput loop on this GPU; the softmax takes one per score
+SFU_EXP2_PER_CLK_SM = 32
 
 
 def head_range(rank, world, H):
@@ -397,6 +400,10 @@ def run_ours(args, w, rank, world):
     max_mhz = ck["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
     med_mhz = ck["sm_mhz"] or max_mhz
     dense = lambda mhz: n_sm * DENSE_BF16_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+    exps_rank = flops_rank / (4 * d)  # one exponential per score
+    sfu_rate = exps_rank / (pair_ms * 1e-3 * med_mhz * 1e6 * n_sm)
+    rope_bytes = (2 * B * N * H * d * (2 if dtype == torch.bfloat16 else 4)) if w.rope else 0
+    t_min_ms = (flops_rank / (tc_burst * 1e12) + (mbytes + rope_bytes) / (hbm * 1e9)) * 1e3
     timed_s = total_ms / 1e3
     line = {
         "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": K,
@@ -429,6 +436,15 @@ def run_ours(args, w, rank, world):
                      "frac_of_dense_at_max_clock": round(achieved / dense(max_mhz), 4),
                      "dense_rate": f"{n_sm} SMs x {DENSE_BF16_FLOP_PER_CLK_SM} bf16 flop/clk "
                                    "(a 128x128x16 tcgen05.mma every 64 cycles, measured)"},
+        "sfu": {"exps_per_launch": exps_rank,
+                "achieved_per_clk_per_sm": round(sfu_rate, 2),
+                "peak_per_clk_per_sm": SFU_EXP2_PER_CLK_SM,
+                "frac": round(sfu_rate / SFU_EXP2_PER_CLK_SM, 4),
+                "clock": "sampled median SM clock of the timed region"},
+        "step_roofline": {"t_min_ms": round(t_min_ms, 4), "frac": round(t_min_ms / ms, 4),
+                          "sum_of": "pair flops at the measured bf16 burst rate + merge and "
+                                    "RoPE (k read and written) bytes at the measured copy "
+                                    "bandwidth"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": hbm,
                            "unit": "GB/s", "frac": round(merge_gbs / hbm, 4),
                            "frac_of_8tbs": round(merge_gbs / 8000.0, 4),
