@@ -378,6 +378,19 @@ def run_ours(args, w, rank, world):
     first_kernel_ms = {name: round(statistics.median(fev[c][x].elapsed_time(fev[c][x + 1])
                                                      for c in range(3)), 4)
                        for x, name in enumerate(("rope", "pair", "merge"))}
+    # two cycles of the workload's schedule (an anchor, then reuse steps until the next one),
+    # each timed as a whole: the mean step over a cycle, against computing every pair each step
+    sched = [wl.step_mask(w, t) for t in range(len(w.schedule))]
+    period = next((t for t in range(1, len(sched)) if not sched[t].any()), len(sched))
+    cycle_ms = []
+    for _ in range(2):
+        ev[0].record()
+        for t in range(period):
+            step(sched[t])
+        ev[1].record()
+        torch.cuda.synchronize()
+        cycle_ms.append(ev[0].elapsed_time(ev[1]) / period)
+    cycle = statistics.mean(cycle_ms)
     esz = 2 if dtype == torch.bfloat16 else 4
     # bytes of the whole job (every rank copies its own heads)
     h2d = 3 * B * N * w.H * d * esz
@@ -421,6 +434,9 @@ def run_ours(args, w, rank, world):
         "anchor_ms": round(statistics.median(anchor_ms), 4),
         "first_reuse_step_ms": round(first_reuse_ms, 4),
         "first_reuse_kernel_ms": first_kernel_ms,
+        "schedule_cycle": {"period": period, "ms_per_step": round(cycle, 4),
+                           "dense_ms_per_step": round(statistics.median(anchor_ms), 4),
+                           "speedup_vs_dense": round(statistics.median(anchor_ms) / cycle, 3)},
         "group_states": bool(args.group),
         "anchor_effective_tflops": round(pair_flops(w, anchor) / (statistics.median(anchor_ms) * 1e-3) / 1e12, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_burst,
