@@ -171,7 +171,9 @@ int ditango_plan(int64_t N, int32_t P, const uint8_t* mask, ditango_plan_t* out_
 /* Frees the plan (host memory only). NULL is accepted. */
 void ditango_plan_destroy(ditango_plan_t plan);
 
-/* Replaces the default reuse mask (same validation as ditango_plan). */
+/* Replaces the default reuse mask (same validation as ditango_plan). The default mask is used
+ * by steps given reuse_mask = NULL, and names the group states an all-compute step builds in
+ * advance (see ditango_state_cache). */
 int ditango_plan_set_mask(ditango_plan_t plan, const uint8_t* mask);
 
 /* Checks `mask` (NULL = default mask) against the bookkeeping without changing anything:
