@@ -12,8 +12,12 @@ tensor), so no L2 flush is needed between steps. `--workload wan14b_layer` times
 Wan2.1-14B-shaped layer (N=32760, P=8) instead.
 
 Prints one JSON line: ms per step (lower is better) plus effective TFLOP/s counted over
-computed pairs only, the pair kernel's roofline against the measured tensor-core peak, per-kernel
-times, an end-to-end number with host buffers, clocks, and the CPU oracle baseline.
+computed pairs only, the pair kernel's roofline against the measured tensor-core peak, its SFU
+rate, the merge's roofline against the measured copy bandwidth, the step's roofline time,
+per-kernel times, the anchor and the first reuse step after it, a whole schedule cycle
+(anchor + reuse steps) against computing every pair, the reuse-fraction sweep, the cycle with
+the far states in host storage, an end-to-end number with host buffers, clocks, and the CPU
+oracle baseline.
 
 With --gpus N (under torchrun) the layer's heads are split across the ranks: rank r computes
 heads [r*H/N, (r+1)*H/N) of the same layer (every (b, h) is independent, so no data crosses
