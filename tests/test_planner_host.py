@@ -94,3 +94,52 @@ def test_set_cache_state_round_trip_and_checks():
         assert e.value.name == "INVALID_ARG"
     v3, sc3, st3 = plan.cache_state()  # unchanged by the refused calls
     assert np.array_equal(v3, valid) and np.array_equal(sc3, sc) and st3 == steps
+
+
+def test_anchor_planner_predicts_the_reuse_mask(monkeypatch):
+    # host logic of AnchorPlanner's ahead-of-time group build, with the device reductions
+    # replaced by fakes: the mask chosen right after an anchor becomes the plan's default mask
+    # before the next anchor, and only when build_ahead is on
+    import torch
+
+    P = 4
+    chosen = [np.array(m, np.uint8) for m in ([[0, 1, 1, 1], [1, 0, 1, 1], [1, 1, 0, 1], [1, 1, 1, 0]],
+                                              [[0, 0, 1, 1], [0, 0, 0, 1], [1, 0, 0, 0], [1, 1, 0, 0]])]
+    calls = {"select": 0}
+
+    def fake_select(plan, w, delta, tau, group, budget):
+        calls["select"] += 1
+        return chosen[(calls["select"] - 1) % 2]
+
+    monkeypatch.setattr(dt, "planner_importance", lambda *a, **k: torch.zeros((P, P)))
+    monkeypatch.setattr(dt, "planner_snapshot", lambda *a, **k: None)
+    monkeypatch.setattr(dt, "planner_drift", lambda *a, **k: torch.zeros(P))
+    monkeypatch.setattr(dt, "planner_select", fake_select)
+
+    class FakePlan:
+        def __init__(self):
+            self.P, self.defaults = P, []
+
+        def set_mask(self, m):
+            self.defaults.append(np.array(m, np.uint8))
+
+    cO = torch.empty((1, 1, P, 8, 4))
+    cL = torch.empty((1, 1, P, 8))
+    for ahead in (True, False):
+        plan = FakePlan()
+        calls["select"] = 0
+        ap = dt.AnchorPlanner(plan, cO, cL, anchor_every=3, tau=1e-3, build_ahead=ahead)
+        masks = []
+        for _ in range(7):
+            m = ap.mask()
+            masks.append(m)
+            ap.after_step(m)
+        assert [bool(m.any()) for m in masks] == [False, True, True, False, True, True, False]
+        if ahead:
+            # anchors at steps 3 and 6 set the mask chosen right after the anchors at 0 and 3
+            assert len(plan.defaults) == 2
+            assert np.array_equal(plan.defaults[0], masks[1])
+            assert np.array_equal(plan.defaults[1], masks[4])
+            assert np.array_equal(ap.predicted, masks[4])
+        else:
+            assert plan.defaults == []
