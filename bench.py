@@ -711,6 +711,21 @@ class OracleBaseline:
                 f"extrapolated x{w.H * w.B} (RoPE) and x{w.B * w.H * w.N / self.rows_n:.0f} (rows)")
 
 
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo), or the platform's processor string."""
+    import platform
+
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip().lower() in ("model name", "cpu model", "hardware"):
+                    return val.strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, steps):
     """The oracle's extrapolated step time: median over `steps` timed sample steps."""
     base = OracleBaseline(w)
@@ -746,6 +761,7 @@ def run_reference(args, w, world=1):
         "config": config_of(w, world),
         "effective_tflops": round(flops / (ms * 1e-3) / 1e12, 6),
         "cpu_baseline": {"value": round(ms, 2), "unit": "ms", "cores": base.nthreads,
+                         "cpu": cpu_model(),
                          "kind": "oracle", "sample": base.sample_text()},
         "e2e": {"value": round(ms, 2), "unit": "ms", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -796,7 +812,7 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             base, est_ms, spent = cpu_baseline(w, args.cpu_steps)
             line["cpu_baseline"] = {"value": round(est_ms, 1), "unit": "ms",
-                                    "cores": base.nthreads, "kind": "oracle",
+                                    "cores": base.nthreads, "cpu": cpu_model(), "kind": "oracle",
                                     "sample": base.sample_text(),
                                     "seconds_spent": round(spent, 1)}
         print(json.dumps(line), flush=True)
