@@ -723,6 +723,14 @@ def cpu_model():
                     return val.strip()
     except OSError:
         pass
+    try:  # Arm hosts name the core in lscpu only
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key, _, val = line.partition(":")
+            if key.strip().lower() == "model name":
+                return val.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     return platform.processor() or platform.machine()
 
 
