@@ -416,6 +416,8 @@ def run_ours(args, w, rank, world):
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     max_mhz = ck["sm_max_mhz"] or peaks.get("sm_max_mhz", 2070.0)
     med_mhz = ck["sm_mhz"] or max_mhz
+    # the pair kernel's head-dim-64 build (SFU rate taken at the timed region's median clock)
+    d64 = head_dim_64(dev, med_mhz) if (args.sweep and world == 1) else None
     dense = lambda mhz: n_sm * DENSE_BF16_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
     exps_rank = flops_rank / (4 * d)  # one exponential per score
     sfu_rate = exps_rank / (pair_ms * 1e-3 * med_mhz * 1e6 * n_sm)
@@ -474,6 +476,7 @@ def run_ours(args, w, rank, world):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": world * K * (3 if w.rope else 2),  # all ranks
         "reuse_sweep": sweep,
+        "head_dim_64": d64,
         "host_storage": offload,
         "clocks": ck,
     }
@@ -551,6 +554,58 @@ def offload_cycle(w, q, k, v, dev, cycles=2):
             "steady_step_ms": round(statistics.median(times[2:]), 4) if period > 2 else None,
             "ms_per_step_over_cycle": round(sum(times) / period, 4),
             "schedule": f"anchor every {period} steps, |i-j|>={D} reused"}
+
+
+def head_dim_64(dev, med_mhz, steps=10):
+    """The pair kernel at head dim 64 (its other build): N = 32760 (21x30x52), H = 40, d = 64,
+    bf16, P = 8, no RoPE, |i - j| >= 2 reused, group states on; seeded N(0,1) inputs. At d = 64
+    a tile's P V and Q K^T take half the tensor time of d = 128 while its softmax (one SFU
+    exponential per score) stays the same, so the SFU rate is reported beside the tensor one."""
+    import numpy as np
+    import torch
+
+    import attention_state_reuse_gb300 as dt
+    from attention_state_reuse_gb300 import workloads as wl
+
+    w = wl.Workload("d64_layer", 5, 1, 40, 64, 21, 30, 52, 8, "bf16", 2, 0.0,
+                    schedule=[("all",), ("dist", 2)])
+    q, k, v = (torch.from_numpy(a).to(dev).to(torch.bfloat16) for a in wl.InputStream(w).next())
+    out = torch.empty_like(q)
+    out_lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    mask = wl.distance_mask(w.P, 2)
+    plan = dt.Plan(w.N, w.P, mask=mask)
+    cO, cL = dt.new_state_cache(w.B, w.H, w.P, w.N, w.d, torch.bfloat16, dev)
+    grp = dt.new_group_state(w.B, w.H, w.N, w.d, dev)
+    step = lambda m: dt.attn_step(plan, q, k, v, cO, cL, out, out_lse, reuse_mask=m,
+                                  softmax_scale=w.scale, group=grp)
+    step(np.zeros((w.P, w.P), np.uint8))
+    step(mask)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for evs in kev:
+        for e in evs:
+            e.record()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for x in range(steps):
+        plan.set_profile_events(kev[x])
+        step(mask)
+    t1.record()
+    plan.set_profile_events(None)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    pair_ms = statistics.median(kev[x][1].elapsed_time(kev[x][2]) for x in range(steps))
+    f = pair_flops(w, mask)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks, _ = load_peaks()
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    tflops = f / (pair_ms * 1e-3) / 1e12
+    sfu = f / (4 * w.d) / (pair_ms * 1e-3 * med_mhz * 1e6 * n_sm)
+    return {"workload": "N=32760 (21x30x52), H=40, d=64, P=8, bf16, no RoPE, |i-j|>=2 reused",
+            "ms": round(ms, 4), "pair_ms": round(pair_ms, 4), "pair_tflops": round(tflops, 1),
+            "pair_frac_of_burst": round(tflops / burst, 4),
+            "sfu_per_clk_per_sm": round(sfu, 2),
+            "sfu_frac": round(sfu / SFU_EXP2_PER_CLK_SM, 4)}
 
 
 def reuse_sweep(dev, steps=10, use_group=True):
