@@ -402,6 +402,7 @@ def run_ours(args, w, rank, world):
 
     sweep = reuse_sweep(dev, use_group=args.group) if (args.sweep and world == 1) else None
     offload = offload_cycle(w, q, k, v, dev) if (args.offload and world == 1) else None
+    planned = planner_cycle(w, q, k, v, dev) if (args.sweep and world == 1) else None
 
     flops = pair_flops(w, mask)            # the whole layer
     flops_rank = flops * H / w.H           # this rank's heads
@@ -478,6 +479,7 @@ def run_ours(args, w, rank, world):
         "reuse_sweep": sweep,
         "head_dim_64": d64,
         "host_storage": offload,
+        "planner": planned,
         "clocks": ck,
     }
     return line
@@ -606,6 +608,87 @@ def head_dim_64(dev, med_mhz, steps=10):
             "pair_frac_of_burst": round(tflops / burst, 4),
             "sfu_per_clk_per_sm": round(sfu, 2),
             "sfu_frac": round(sfu / SFU_EXP2_PER_CLK_SM, 4)}
+
+
+def planner_cycle(w, q, k, v, dev, cycles=2, anchor_every=4, tau=1e-3, group=2, sigma=0.02):
+    """The anchor-guided planner driving the layer: AnchorPlanner chooses every step's mask
+    (anchors every `anchor_every` steps, threshold tau, groups of `group` KV partitions) while
+    the inputs drift, x_t = x_0 + sigma * t * eps (eps ~ N(0,1), seeded, made on the device
+    before timing). Times `cycles` cycles as a whole (CUDA events and the host clock: the
+    planner reads the drift back to the host each step), and each planner part once: the
+    anchor's importance and snapshot, the per-step drift and the host selection."""
+    import numpy as np
+    import torch
+
+    import attention_state_reuse_gb300 as dt
+
+    B, N, H, d, P = w.B, w.N, q.shape[2], w.d, w.P
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 * w.index + 900)
+    steps = cycles * anchor_every
+    eps = [torch.randn(q.shape, generator=gen, device=dev, dtype=torch.float32) for _ in range(3)]
+    drifted = [[(x.float() + sigma * t * e).to(q.dtype) for x, e in zip((q, k, v), eps)]
+               for t in range(anchor_every)]
+    del eps
+    plan = dt.Plan(N, P)
+    cO, cL = dt.new_state_cache(B, H, P, N, d, q.dtype, dev)
+    grp = dt.new_group_state(B, H, N, d, dev)
+    out = torch.empty_like(q)
+    out_lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    rope = None
+    if w.rope:
+        dtt, dhh, dww = w.rope_dims
+        rope = dt.RopeTables(w.start_frame + w.T, w.Hl, w.Wl, dtt, dhh, dww,
+                             start_frame=w.start_frame, device=dev)
+    ws = torch.empty(max(1, dt.workspace_size(plan, B, H, d, q.dtype, w.rope)), dtype=torch.uint8,
+                     device=dev)
+    ap = dt.AnchorPlanner(plan, cO, cL, anchor_every=anchor_every, tau=tau, group=group)
+
+    def run(n):
+        fracs = []
+        for t in range(n):
+            m = ap.mask()
+            qq, kk, vv = drifted[t % anchor_every]
+            dt.attn_step(plan, qq, kk, vv, cO, cL, out, out_lse, reuse_mask=m, rope=rope,
+                         softmax_scale=w.scale, workspace=ws, group=grp)
+            ap.after_step(m)
+            fracs.append(float(np.asarray(m).mean()))
+        return fracs
+
+    run(steps)  # warm-up cycles (the planner's first anchor has no prediction yet)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
+    e0.record()
+    fracs = run(steps)
+    e1.record()
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - h0) * 1e3 / steps
+    dev_ms = e0.elapsed_time(e1) / steps
+    st = dt.device_status()
+    if st != (0, 0):
+        raise RuntimeError(f"device status after the planner cycle: {st}")
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        r = fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b), r
+
+    imp_ms, wgt = timed(lambda: dt.planner_importance(plan, cO, cL))
+    snap_ms, _ = timed(lambda: dt.planner_snapshot(plan, cO, cL, ap.snapshot))
+    drift_ms, delta = timed(lambda: dt.planner_drift(plan, cO, cL, ap.snapshot))
+    wn, dn = wgt.cpu().numpy(), delta.cpu().numpy()
+    h0 = time.perf_counter()
+    dt.planner_select(plan, wn, dn, tau, group)
+    select_ms = (time.perf_counter() - h0) * 1e3
+    return {"anchor_every": anchor_every, "tau": tau, "group": group, "drift_sigma": sigma,
+            "ms_per_step": round(dev_ms, 4), "wall_ms_per_step": round(wall_ms, 4),
+            "reuse_fraction_per_step": [round(f, 4) for f in fracs[:anchor_every]],
+            "importance_ms": round(imp_ms, 4), "snapshot_ms": round(snap_ms, 4),
+            "drift_ms": round(drift_ms, 4), "select_host_ms": round(select_ms, 4)}
 
 
 def reuse_sweep(dev, steps=10, use_group=True):
