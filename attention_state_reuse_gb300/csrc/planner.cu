@@ -102,46 +102,90 @@ __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
   x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
 }
 
-// One thread per row r of (b, h) = blockIdx.y: sum over the row's d channels of
-// (O_ii - O_ii(anchor))^2 and O_ii(anchor)^2, i = partition(r), into the block's 2P sums.
+// Sums of row r's (O_ii - O_ii(anchor))^2 and O_ii(anchor)^2 over this thread's 8 channels
+// c0..c0+7 of (b, h) slab bh, i = partition(r).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) drift_kernel(const __grid_constant__ PlannerArgs a) {
+__device__ __forceinline__ void drift_terms(const PlannerArgs& a, int64_t bh, int i, int64_t r,
+                                            int c0, float& num, float& den) {
+  T* o;
+  float* l;
+  state_ptrs(a.cache, a.P, a.N, a.d, bh, i, i, r, o, l);  // the local state (i, i)
+  const T* ref = static_cast<const T*>(a.snap) + (bh * a.N + r) * a.d;
+  float x[8], y[8];
+  load8(o + c0, x);
+  load8(ref + c0, y);
+  num = den = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float df = x[k] - y[k];
+    num = fmaf(df, df, num);
+    den = fmaf(y[k], y[k], den);
+  }
+}
+
+// A block takes kThreads consecutive rows of (b, h) = blockIdx.y, d/8 threads per row at a
+// time (each over 8 channels, so that a warp reads whole rows, coalesced), in d/8 rounds, into
+// the block's 2P sums, then once per block into the fp64 device sums. When the block's rows
+// lie in at most two partitions (partitions longer than the block), a thread keeps one pair of
+// sums per partition in registers and the block reduces them once at the end, so the rounds'
+// loads do not wait on reductions; otherwise every round is reduced on its own.
+// tpr_shift = log2(d/8).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) drift_kernel(const __grid_constant__ PlannerArgs a,
+                                                         int tpr_shift) {
   __shared__ float acc[2 * kMaxP];
   for (int x = threadIdx.x; x < 2 * a.P; x += kThreads) acc[x] = 0.f;
   __syncthreads();
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  const bool live = r < a.N;
-  const int64_t rr = live ? r : a.N - 1;
-  const int i = partition_of(a, rr);
-  const int i0 = __shfl_sync(0xffffffffu, i, 0);  // every lane takes part, live or not
-  const bool uniform = __all_sync(0xffffffffu, live && i == i0);
+  const int rows_per_round = kThreads >> tpr_shift;
+  const int rounds = 1 << tpr_shift;
+  const int c0 = (threadIdx.x & (rounds - 1)) * 8;
   const int64_t bh = blockIdx.y;
-  const T* cur;
-  {
-    T* o;
-    float* l;
-    state_ptrs(a.cache, a.P, a.N, a.d, bh, i, i, rr, o, l);  // the local state (i, i)
-    cur = o;
-  }
-  const T* ref = static_cast<const T*>(a.snap) + (bh * a.N + rr) * a.d;
-  float num = 0.f, den = 0.f;
-  for (int c = 0; c < a.d; c += 8) {
-    float x[8], y[8];
-    load8(cur + c, x);
-    load8(ref + c, y);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float df = x[k] - y[k];
-      num = fmaf(df, df, num);
-      den = fmaf(y[k], y[k], den);
+  const int64_t r_first = static_cast<int64_t>(blockIdx.x) * kThreads;
+  const int64_t r_last = (r_first + kThreads < a.N ? r_first + kThreads : a.N) - 1;
+  const int ia = partition_of(a, r_first), ib = partition_of(a, r_last);  // block-uniform
+  if (ib - ia <= 1) {
+    const int64_t split = a.offsets[ib];  // first row of partition ib
+    float na = 0.f, da = 0.f, nb = 0.f, db = 0.f;
+#pragma unroll 4
+    for (int round = 0; round < rounds; ++round) {
+      const int64_t r = r_first + round * rows_per_round + (threadIdx.x >> tpr_shift);
+      if (r <= r_last) {
+        const bool in_a = ib == ia || r < split;
+        float num, den;
+        drift_terms<T>(a, bh, in_a ? ia : ib, r, c0, num, den);
+        if (in_a) {
+          na += num;
+          da += den;
+        } else {
+          nb += num;
+          db += den;
+        }
+      }
+    }
+    add_slot(acc, 2 * ia, na, true);
+    add_slot(acc, 2 * ia + 1, da, true);
+    if (ib != ia) {
+      add_slot(acc, 2 * ib, nb, true);
+      add_slot(acc, 2 * ib + 1, db, true);
+    }
+  } else {
+    for (int round = 0; round < rounds; ++round) {
+      const int64_t r = r_first + round * rows_per_round + (threadIdx.x >> tpr_shift);
+      const bool live = r <= r_last;
+      const int64_t rr = live ? r : r_last;
+      const int i = partition_of(a, rr);
+      const int i0 = __shfl_sync(0xffffffffu, i, 0);  // every lane takes part, live or not
+      const bool uniform = __all_sync(0xffffffffu, live && i == i0);
+      float num, den;
+      drift_terms<T>(a, bh, i, rr, c0, num, den);
+      if (!live) num = den = 0.f;
+      add_slot(acc, 2 * i, num, uniform);
+      add_slot(acc, 2 * i + 1, den, uniform);
     }
   }
-  if (!live) num = den = 0.f;
-  add_slot(acc, 2 * i, num, uniform);
-  add_slot(acc, 2 * i + 1, den, uniform);
   __syncthreads();
-  for (int x = threadIdx.x; x < 2 * a.P; x += kThreads)
-    if (acc[x] != 0.f) atomicAdd(a.sums + x, static_cast<double>(acc[x]));
+  for (int x2 = threadIdx.x; x2 < 2 * a.P; x2 += kThreads)
+    if (acc[x2] != 0.f) atomicAdd(a.sums + x2, static_cast<double>(acc[x2]));
 }
 
 // One thread, in ascending i: out[i] may share storage with sums (the caller's buffer holds
@@ -170,12 +214,15 @@ cudaError_t launch_planner_importance(const PlannerArgs& a, cudaStream_t stream)
 cudaError_t launch_planner_drift(const PlannerArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(a.sums, 0, 2 * static_cast<size_t>(a.P) * sizeof(double), stream);
   if (e != cudaSuccess) return e;
+  const int tpr = a.d / 8;  // threads per row
+  if (a.d % 8 != 0 || tpr < 1 || tpr > 32 || (tpr & (tpr - 1)) != 0) return cudaErrorInvalidValue;
+  const int tpr_shift = 31 - __builtin_clz(static_cast<unsigned>(tpr));
   const dim3 grid(static_cast<unsigned>((a.N + kThreads - 1) / kThreads),
                   static_cast<unsigned>(a.B * a.H));
   if (a.dtype == DITANGO_BF16)
-    drift_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(a);
+    drift_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(a, tpr_shift);
   else
-    drift_kernel<float><<<grid, kThreads, 0, stream>>>(a);
+    drift_kernel<float><<<grid, kThreads, 0, stream>>>(a, tpr_shift);
   drift_finalize<<<1, 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
