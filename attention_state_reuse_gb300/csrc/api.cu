@@ -502,23 +502,11 @@ int ditango_planner_snapshot(ditango_plan_t plan, const ditango_state_cache* cac
   int st = planner_args(plan, cache, &a);
   if (st != DITANGO_OK) return st;
   if ((st = check_snapshot(a, snapshot)) != DITANGO_OK) return st;
-  // rows of partition i in the device slot of (i, i) of every (b, h) (the local pair is always
-  // on the device): one 2-D copy per partition
-  const size_t esz = elem_size(a.dtype);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t S = a.cache.S;
-  for (int32_t i = 0; i < a.P; ++i) {
-    const int64_t off = a.offsets[i], rows = a.offsets[i + 1] - a.offsets[i];
-    const int64_t slot = a.cache.slot[i * a.P + i];
-    const uint8_t* src = static_cast<const uint8_t*>(a.cache.dO) +
-                         static_cast<size_t>((slot * a.N + off) * a.d) * esz;
-    uint8_t* dst = static_cast<uint8_t*>(snapshot->ptr) + static_cast<size_t>(off * a.d) * esz;
-    if (cudaMemcpy2DAsync(dst, static_cast<size_t>(a.N * a.d) * esz, src,
-                          static_cast<size_t>(S * a.N * a.d) * esz,
-                          static_cast<size_t>(rows * a.d) * esz, static_cast<size_t>(a.B * a.H),
-                          cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-      return DITANGO_ERR_CUDA;
-  }
+  // rows of partition i from the device slot of (i, i) of every (b, h) (the local pair is
+  // always on the device), by a copy kernel
+  a.snap = snapshot->ptr;
+  if (launch_planner_snapshot(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DITANGO_ERR_CUDA;
   return DITANGO_OK;
 }
 

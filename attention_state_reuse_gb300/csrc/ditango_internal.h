@@ -162,6 +162,7 @@ struct PlannerArgs {
 };
 cudaError_t launch_planner_importance(const PlannerArgs& args, cudaStream_t stream);
 cudaError_t launch_planner_drift(const PlannerArgs& args, cudaStream_t stream);
+cudaError_t launch_planner_snapshot(const PlannerArgs& args, cudaStream_t stream);
 
 // 3D RoPE applied to up to two [B, N, H, d] tensors, written contiguous.
 struct RopeApplyArgs {

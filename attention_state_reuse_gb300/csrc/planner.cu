@@ -188,6 +188,35 @@ __global__ void __launch_bounds__(kThreads) drift_kernel(const __grid_constant__
     if (acc[x2] != 0.f) atomicAdd(a.sums + x2, static_cast<double>(acc[x2]));
 }
 
+// The snapshot: row r of (b, h) = blockIdx.y copied from its local state (i, i) (a device
+// slot) into snap [B, H, N, d]. Same thread layout as drift_kernel: 256 rows per block, d/8
+// threads per row at a time, 8 elements (16 or 32 bytes) per thread and round.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) snapshot_kernel(const __grid_constant__ PlannerArgs a,
+                                                            int tpr_shift) {
+  constexpr int V = 8 * static_cast<int>(sizeof(T)) / 16;  // 16-byte vectors per thread
+  const int rows_per_round = kThreads >> tpr_shift;
+  const int rounds = 1 << tpr_shift;
+  const int c0 = (threadIdx.x & (rounds - 1)) * 8;
+  const int64_t bh = blockIdx.y;
+  const int64_t r_first = static_cast<int64_t>(blockIdx.x) * kThreads;
+#pragma unroll 4
+  for (int round = 0; round < rounds; ++round) {
+    const int64_t r = r_first + round * rows_per_round + (threadIdx.x >> tpr_shift);
+    if (r >= a.N) continue;
+    const int i = partition_of(a, r);
+    T* o;
+    float* l;
+    state_ptrs(a.cache, a.P, a.N, a.d, bh, i, i, r, o, l);
+    const uint4* src = reinterpret_cast<const uint4*>(o + c0);
+    // the snapshot is the one buffer this launch writes (const in the args, shared with drift)
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(const_cast<void*>(a.snap)) +
+                                          (bh * a.N + r) * a.d + c0);
+#pragma unroll
+    for (int v = 0; v < V; ++v) dst[v] = __ldg(src + v);
+  }
+}
+
 // One thread, in ascending i: out[i] may share storage with sums (the caller's buffer holds
 // the 2P sums, then the P drifts), and position i is never read again once i is done.
 __global__ void drift_finalize(const __grid_constant__ PlannerArgs a) {
@@ -224,6 +253,19 @@ cudaError_t launch_planner_drift(const PlannerArgs& a, cudaStream_t stream) {
   else
     drift_kernel<float><<<grid, kThreads, 0, stream>>>(a, tpr_shift);
   drift_finalize<<<1, 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_planner_snapshot(const PlannerArgs& a, cudaStream_t stream) {
+  const int tpr = a.d / 8;  // threads per row
+  if (a.d % 8 != 0 || tpr < 1 || tpr > 32 || (tpr & (tpr - 1)) != 0) return cudaErrorInvalidValue;
+  const int tpr_shift = 31 - __builtin_clz(static_cast<unsigned>(tpr));
+  const dim3 grid(static_cast<unsigned>((a.N + kThreads - 1) / kThreads),
+                  static_cast<unsigned>(a.B * a.H));
+  if (a.dtype == DITANGO_BF16)
+    snapshot_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(a, tpr_shift);
+  else
+    snapshot_kernel<float><<<grid, kThreads, 0, stream>>>(a, tpr_shift);
   return cudaGetLastError();
 }
 
