@@ -202,6 +202,18 @@ def test_reuse_sweep_every_mask(P):
     assert len(errs) == len(w.schedule) == P + 1 - {4: 1, 8: 1, 16: 2}[P] + 1
 
 
+def test_maximum_partitions_full_length():
+    # the largest plan (P = 64) over a full-length sequence (N = 32760, 511-512 rows per
+    # partition: two units per (b, h, i), the second with a ragged second tile), RoPE, random
+    # masks and changing distance masks, group states on, two heads
+    base = wl.get("wan14b_layer")
+    sched = [("all",), ("random",), ("dist", 5), ("dist", 5), ("random",), ("all",), ("dist", 2)]
+    w = wl.Workload("p64_full", 7, 1, 2, 128, base.T, base.Hl, base.Wl, 64, "bf16", len(sched),
+                    0.02, rope=True, schedule=sched)
+    pr = ParityRun(w, rows=sample_rows(w, range(w.H), per_partition_random=1), group=True)
+    run_all_steps(pr)
+
+
 # ------------------------------------------------------------------- merge entry point
 @pytest.mark.parametrize("dtype,n,d", [(torch.bfloat16, 1, 128), (torch.bfloat16, 7, 64),
                                        (torch.bfloat16, 64, 128), (torch.float32, 5, 64),
